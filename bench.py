@@ -1,0 +1,452 @@
+"""Benchmark of the packed index step (score + block top-k) on GB300.
+
+One step = one idx_score_topk call (score kernel + top-k kernel) over the whole
+synthetic batch of the workload, with the batch resident in HBM.  Prints ONE
+JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the
+method) on a bounded sample of the same workload, on this host's cores; it is
+the reference arm (the pages' own kernels are not available to run).
+Multi-GPU runs (torchrun) are independent replicas: each rank scores its own
+copy of the workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "index-step µs/layer and achieved HBM GB/s (score+top-k), 16 req × 131K bf16"
+DEFAULT_WORKLOAD = "bf16_16x131k"
+PUBLISHED_US = {"bf16_16x131k": 119.1, "fp8_16x131k": 87.4}   # packed kernel, one GB300 rank
+BYTES_PER_TOKEN = {"bf16": 256, "fp8_e4m3": 132, "nvfp4": 72}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+SCORE_SOURCES = ["idx_score.cu", "idx_ptx.cuh", "idx_internal.cuh"]
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in SCORE_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return 6800.0, "fallback 6.8 TB/s"
+
+
+def algorithmic_bytes(batch) -> dict:
+    """Bytes the score kernel must move at minimum: each request's keys read once
+    up to its longest row, plus q, the page-table entries and slot/length
+    metadata, plus the block-max writes; the top-k reads the block maxima back
+    and writes the outputs."""
+    s = batch.spec
+    lens = batch.group_lens()
+    k_bytes = sum(lens) * BYTES_PER_TOKEN[s.k_dtype]
+    q_bytes = batch.q.numel() * batch.q.element_size() + (0 if batch.q_scale is None else batch.q_scale.numel() * 4)
+    pages = sum((L + 63) // 64 for L in lens)
+    meta = pages * 4 + batch.R * 4 + batch.row_lens.numel() * 4
+    bm = 0
+    for r in range(batch.R):
+        if lens[r] == 0:
+            continue
+        for j in range(s.packed_queries):
+            L = int(batch.row_lens[r, j])
+            bm += s.gqa * max(0, (L + 127) // 128) * 4
+    out = batch.R * batch.M * s.topk * 8
+    return {"score": k_bytes + q_bytes + meta + bm, "keys": k_bytes, "topk": bm + out}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.dev = device_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, dev) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    import sparse_attention_indexer_packed_gb300 as idx
+    from sparse_attention_indexer_packed_gb300.build import build_library
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build_library()
+
+    spec = workloads.WORKLOADS[args.workload]
+    if ws_n > 1:
+        spec = workloads.Spec(**{**spec.__dict__, "seed": spec.seed + 100 * rank})
+    batch = workloads.make_batch(spec)
+    s = batch.spec
+    payload = batch.payload.to(dev)
+    scale = None if batch.scale is None else batch.scale.to(dev)
+    if s.k_dtype == "nvfp4":
+        idx.idx_store_nvfp4(batch.staging.to(dev), batch.slot_mapping.to(dev), (payload, scale))
+        batch.staging = None
+    q = batch.q.to(dev)
+    q_scale = None if batch.q_scale is None else batch.q_scale.to(dev)
+    pt = batch.page_table.to(dev)
+    slots = batch.slot_ids.to(dev)
+    lens = batch.row_lens.to(dev)
+    R, M, topk = batch.R, batch.M, s.topk
+    out_ids = torch.empty((R, M, topk), dtype=torch.int32, device=dev)
+    out_sc = torch.empty((R, M, topk), dtype=torch.float32, device=dev)
+    wsp = idx.alloc_workspace(R, s.packed_queries, s.gqa, batch.max_pages, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        if events is not None:
+            idx.idx_set_kernel_events(*events)
+        idx.idx_score_topk(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
+                           s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, topk,
+                           out_ids, out_sc, wsp, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    flags = idx.idx_workspace_errors(wsp)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during warm-up")
+
+    # ---- timed region: K steps, per-kernel events on the launching stream -----
+    # torch creates an event's CUDA handle on its first record(); record each once
+    # here so the library can re-record the same handles inside the timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for trio in evs:
+        for e in trio:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(ws_n)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws_n)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), ws_n, dev)
+    score_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    topk_ms = [e[1].elapsed_time(e[2]) for e in evs]
+
+    # ---- end to end through the public API with host buffers ------------------
+    e2e = run_e2e(idx, batch, payload, scale, dev, stream, args)
+
+    ab = algorithmic_bytes(batch)
+    score_avg_ms = sum(score_ms) / len(score_ms)
+    achieved = ab["score"] / (score_avg_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            tr = json.load(fh).get(args.workload)
+        if tr and tr.get("kernel_sha") == kernel_sha():
+            traffic = tr["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    ms_per_step = total_ms / args.steps
+    value = ms_per_step * 1e3 / 1.0   # µs per step on each rank (replicas run concurrently)
+    line = {
+        "metric": METRIC if args.workload == DEFAULT_WORKLOAD else f"index-step µs/layer ({args.workload})",
+        "value": round(value, 3),
+        "unit": "us",
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": (round(value / PUBLISHED_US[args.workload], 4)
+                        if args.workload in PUBLISHED_US else None),
+        "dtype": {"bf16": "bf16", "fp8_e4m3": "e4m3", "nvfp4": "e2m1xe4m3/bf16"}[s.k_dtype],
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "requests": R, "packed_queries": s.packed_queries,
+            "gqa": s.gqa, "k_dtype": s.k_dtype, "q_dtype": s.q_dtype,
+            "context": (f"U[{s.len_range[0]},{s.len_range[1]}]" if s.len_range else "explicit"),
+            "topk": topk, "init_blocks": s.init_blocks, "local_blocks": s.local_blocks,
+            "block": 128, "page": 64, "parallelism": f"replicas x{ws_n}",
+            "l2": f"inputs larger than L2 ({ab['keys'] / 1e6:.0f} MB of keys read per step), no flush",
+            "aggregate_GBps": round(ws_n * ab["score"] / (ms_per_step * 1e-3) / 1e9, 1),
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "score_kernel", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": peak_src, "traffic": traffic,
+            "algorithmic_bytes_per_launch": ab["score"],
+            "score_us": round(score_avg_ms * 1e3, 3), "topk_us": round(sum(topk_ms) / len(topk_ms) * 1e3, 3),
+            "frac_of_8TBps": round(achieved / 8000.0, 4),
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(batch, args) if ws_n == 1 else None
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(idx, batch, payload, scale, dev, stream, args):
+    """Same step through the public API, inputs copied from pinned host memory
+    and outputs read back, all inside the timed region."""
+    s = batch.spec
+    hq = batch.q.pin_memory()
+    hqs = None if batch.q_scale is None else batch.q_scale.pin_memory()
+    hpt = batch.page_table.pin_memory()
+    hsl = batch.slot_ids.pin_memory()
+    hln = batch.row_lens.pin_memory()
+    R, M, topk = batch.R, batch.M, s.topk
+    hid = torch.empty((R, M, topk), dtype=torch.int32).pin_memory()
+    hsc = torch.empty((R, M, topk), dtype=torch.float32).pin_memory()
+    dq = torch.empty_like(hq, device=dev)
+    dqs = None if hqs is None else torch.empty_like(hqs, device=dev)
+    dpt = torch.empty_like(hpt, device=dev)
+    dsl = torch.empty_like(hsl, device=dev)
+    dln = torch.empty_like(hln, device=dev)
+    did = torch.empty((R, M, topk), dtype=torch.int32, device=dev)
+    dsc = torch.empty((R, M, topk), dtype=torch.float32, device=dev)
+    wsp = idx.alloc_workspace(R, s.packed_queries, s.gqa, batch.max_pages, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in [hq, hpt, hsl, hln] + ([hqs] if hqs is not None else []))
+    d2h = hid.numel() * 4 + hsc.numel() * 4
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        if dqs is not None:
+            dqs.copy_(hqs, non_blocking=True)
+        dpt.copy_(hpt, non_blocking=True)
+        dsl.copy_(hsl, non_blocking=True)
+        dln.copy_(hln, non_blocking=True)
+        idx.idx_score_topk(dq, dqs, payload, scale, s.k_dtype, dpt, dsl, dln, s.packed_queries,
+                           s.gqa, s.init_blocks, s.local_blocks, topk, did, dsc, wsp, stream)
+        hid.copy_(did, non_blocking=True)
+        hsc.copy_(dsc, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(10, min(args.steps, 200))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = t0.elapsed_time(t1) * 1e3 / n
+    return {"value": round(us, 3), "unit": "us", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n,
+            "note": "keys stay resident in the pool (a layer's index-K cache); q, page table, "
+                    "slot ids and row lengths are copied in, ids and scores copied out"}
+
+
+def _oracle_sample(batch, budget_s: float):
+    """Time the oracle on request 0 with its rows cut to n tokens; returns
+    (seconds per token-row, n, cores)."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _util import oracle_kwargs
+    s = batch.spec
+    kw = oracle_kwargs(batch)
+    r0 = next(r for r in range(batch.R) if batch.group_lens()[r] > 0)
+    n = 4096
+    while True:
+        lens = np.minimum(kw["row_lens"][r0:r0 + 1], n)
+        kw1 = dict(kw, q=kw["q"][r0:r0 + 1], q_scale=None if kw["q_scale"] is None else kw["q_scale"][r0:r0 + 1],
+                   slot_ids=kw["slot_ids"][r0:r0 + 1], row_lens=lens)
+        t = time.perf_counter()
+        oracle.index.index_step(**kw1)
+        dt = time.perf_counter() - t
+        tokens = int(lens.sum()) * s.gqa
+        if dt > budget_s / 4 or n >= int(kw["row_lens"][r0].max()):
+            return dt / tokens, n, dt
+        n *= 2
+
+
+def _cores() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return max(int(i.get("num_threads", 1)) for i in info)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(batch, args) -> dict:
+    per_tok, n, dt = _oracle_sample(batch, budget_s=20.0)
+    total_rows = int(sum(batch.row_lens[r].clamp_min(0).sum() for r in range(batch.R)
+                         if batch.group_lens()[r] > 0)) * batch.spec.gqa
+    us = per_tok * total_rows * 1e6
+    return {"value": round(us, 1), "unit": "us", "cores": _cores(), "kind": "oracle",
+            "sample": f"request 0, all {batch.M} packed rows cut to {n} tokens "
+                      f"({dt:.2f} s), scaled by token-rows to the whole step"}
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    spec = workloads.WORKLOADS[args.workload]
+    batch = workloads.make_batch(spec)
+    budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    per_tok, n, dt = _oracle_sample(batch, budget_s=budget * 4)
+    total_rows = int(sum(batch.row_lens[r].clamp_min(0).sum() for r in range(batch.R)
+                         if batch.group_lens()[r] > 0)) * spec.gqa
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _util import oracle_kwargs
+    kw = oracle_kwargs(batch)
+    r0 = next(r for r in range(batch.R) if batch.group_lens()[r] > 0)
+    lens = np.minimum(kw["row_lens"][r0:r0 + 1], n)
+    kw1 = dict(kw, q=kw["q"][r0:r0 + 1], q_scale=None if kw["q_scale"] is None else kw["q_scale"][r0:r0 + 1],
+               slot_ids=kw["slot_ids"][r0:r0 + 1], row_lens=lens)
+    for _ in range(args.warmup):
+        oracle.index.index_step(**kw1)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.index.index_step(**kw1)
+    el = time.perf_counter() - t
+    tokens = int(lens.sum()) * spec.gqa
+    us = el / args.steps / tokens * total_rows * 1e6
+    cores = _cores()
+    sample = (f"per step: request 0, all {batch.M} packed rows cut to {n} tokens; "
+              f"scaled by token-rows to the whole step")
+    line = {
+        "impl": "reference",
+        "metric": METRIC if args.workload == DEFAULT_WORKLOAD else f"index-step µs/layer ({args.workload})",
+        "value": round(us, 1), "unit": "us", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "requests": batch.R},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

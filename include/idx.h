@@ -1,0 +1,213 @@
+/*
+ * libidx — packed sparse-attention index scoring + block top-k for GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer named "device" must point to device memory of the current
+ * CUDA device; "host" pointers are read before the call returns.  Streams are
+ * cudaStream_t values passed as void* (NULL = legacy default stream).  No call
+ * below synchronises the host with the device, except the ones marked "syncs".
+ *
+ * Constants of the format (the pages' workloads):
+ *   page = 64 tokens, block = 128 tokens, head dim D = 128, at most 16 packed rows.
+ *
+ * Pool planes (one index-K pool per layer; ROCm/ATOM #2745, Summary, "Pool and
+ * binding": payload and scale kept as separate uint8 planes):
+ *   payload: uint8 [num_pages * 64][row_bytes], physical row = page * 64 + t % 64
+ *            row_bytes = 256 (bf16 keys, little-endian), 128 (e4m3 codes),
+ *            64 (NVFP4: two e2m1 codes per byte, even element in the low nibble)
+ *   scale:   uint8 [num_pages * 64][scale_bytes]
+ *            scale_bytes = 0 (bf16: no plane), 4 (fp8: one fp32 per key),
+ *            8 (NVFP4: one E4M3 scale per 16 elements, unit outer scale)
+ */
+#ifndef LIBIDX_IDX_H_
+#define LIBIDX_IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define IDX_API __attribute__((visibility("default")))
+#else
+#define IDX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IDX_ABI_VERSION 1
+#define IDX_PAGE_SIZE 64
+#define IDX_BLOCK_SIZE 128
+#define IDX_DIM 128
+#define IDX_MAX_PACKED_ROWS 16
+#define IDX_MAX_TOPK 256
+#define IDX_WORKSPACE_HEADER_BYTES 256
+
+typedef enum {
+  IDX_BF16 = 0,      /* bfloat16 */
+  IDX_FP8_E4M3 = 1,  /* OCP E4M3 ("fn": no infinities, max 448) with fp32 scales */
+  IDX_NVFP4 = 2      /* e2m1 payload + E4M3 per-16 scales (keys only) */
+} idx_dtype;
+
+typedef enum {
+  IDX_OK = 0,
+  IDX_ERR_INVALID = -1,      /* an argument is out of range or a pointer is NULL */
+  IDX_ERR_UNSUPPORTED = -2,  /* a dtype combination this library does not implement */
+  IDX_ERR_CUDA = -3,         /* a CUDA runtime call or kernel launch failed */
+  IDX_ERR_OOM = -4           /* device allocation failed */
+} idx_status;
+
+/* Device-side error flags, OR-ed into the first 4 bytes of the workspace. */
+#define IDX_DEVERR_BAD_PAGE 1u      /* a page id outside [0, num_pages): page not read */
+#define IDX_DEVERR_TIMEOUT 2u       /* a pipeline wait gave up (kernel ended early) */
+#define IDX_DEVERR_LEN_CLAMPED 4u   /* a row longer than max_pages * 64 was clamped */
+
+/* One index-K pool: payload + scale planes of a paged cache. */
+typedef struct idx_pool {
+  int32_t dtype;              /* idx_dtype of the keys */
+  int32_t page_size;          /* tokens per page: 64 */
+  int32_t dim;                /* head dim: 128 */
+  int32_t reserved;
+  int64_t num_pages;
+  void* payload;              /* device, uint8 [num_pages*64][payload_row_bytes] */
+  void* scale;                /* device, uint8 [num_pages*64][scale_row_bytes]; NULL for bf16 */
+  int64_t payload_row_bytes;  /* 256 | 128 | 64 */
+  int64_t scale_row_bytes;    /* 0 | 4 | 8 */
+} idx_pool;
+
+/* Library / status helpers. */
+IDX_API int idx_abi_version(void);
+IDX_API const char* idx_status_string(int status);
+/* Text of the last error raised on the calling host thread ("" if none). */
+IDX_API const char* idx_last_error(void);
+
+/*
+ * idx_pool_alloc — allocate the planes of a paged index-K pool on the current device.
+ * The pool layout is the one the ATOM NVFP4 index cache page describes (ROCm/ATOM
+ * #2745, Summary): 72 B per NVFP4 key (64 B payload + 8 B scales), 128 B + 4 B
+ * per fp8 key, 256 B per bf16 key.  Contents are uninitialised.
+ *   dtype: idx_dtype; num_pages >= 1; page_size must be 64; dim must be 128.
+ *   out (host): filled on success; the library owns the planes until idx_pool_free.
+ * Returns IDX_ERR_INVALID for bad arguments, IDX_ERR_OOM if cudaMalloc fails.
+ */
+IDX_API int idx_pool_alloc(int dtype, int64_t num_pages, int page_size, int dim, idx_pool* out);
+
+/* idx_pool_free — release planes made by idx_pool_alloc (syncs with the device
+ * through cudaFree).  Zeroes *pool.  A pool whose planes the caller allocated must
+ * not be passed here. */
+IDX_API int idx_pool_free(idx_pool* pool);
+
+/*
+ * idx_store_nvfp4 — quantise staged bf16 keys to NVFP4 and write them into the pool
+ * at their real slots (ROCm/ATOM #2745, Summary: "Store" and "Write").  Per group of
+ * 16 elements: amax in fp32; scale = E4M3(amax / 6) rounded half-to-even, saturating
+ * at 448; codes = e2m1(x / scale) with a correctly rounded fp32 division, rounded
+ * half-to-even, saturating at 6, sign kept (a negative value rounding to 0 is 0x8);
+ * a scale of 0 writes all-zero codes; element 2b goes to the low nibble of byte b.
+ *   src_bf16 (device):     bf16 [num_tokens][128], token-major staging buffer.
+ *   slot_mapping (device): int64 [num_tokens], physical pool row of each key
+ *                          (page * 64 + offset); a negative entry skips the key; an
+ *                          entry >= num_pages*64 skips it too.
+ *   pool (host):           an NVFP4 pool (caller- or library-allocated planes).
+ * Asynchronous on stream.  IDX_ERR_INVALID if pool is not NVFP4 or a pointer is NULL
+ * (num_tokens == 0 is a no-op).
+ */
+IDX_API int idx_store_nvfp4(const void* src_bf16, const int64_t* slot_mapping, int64_t num_tokens,
+                    const idx_pool* pool, void* stream);
+
+/*
+ * idx_score_topk_workspace_bytes — device scratch idx_score_topk needs: a 256-byte
+ * header (device error flags) plus one fp32 block score per (request, packed row,
+ * block): num_requests * packed_queries * gqa * ceil(max_pages / 2) floats.
+ */
+IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queries, int gqa,
+                                      int max_pages);
+
+/*
+ * idx_score_topk — the packed index step of one sparse layer (sglang #45451,
+ * Modifications; sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring for EAGLE
+ * verify rows", Modifications 1).
+ *
+ * For request r, its P = packed_queries draft rows times G = gqa heads (P*G <= 16)
+ * form one 16-row tile; tile row i is (draft row i / G, head i % G).  The tile is
+ * dotted with the request's keys, read once per request up to the group's longest
+ * row.  Row i then keeps only tokens t < its own length, takes the max score of each
+ * 128-token block, always keeps its first init_blocks and last local_blocks blocks
+ * (from its own block count), and emits topk block ids with their scores.
+ *
+ *   q (device):          [R][P][G][128] bf16 (q_dtype IDX_BF16) or e4m3 codes (IDX_FP8_E4M3)
+ *   q_scale (device):    fp32 [R][P*G], one scale per packed row; required for e4m3 q,
+ *                        ignored (may be NULL) for bf16 q
+ *   k_payload, k_scale (device): the pool planes; k_scale is ignored for bf16 keys
+ *   k_dtype:             IDX_BF16 (with bf16 q), IDX_FP8_E4M3 (with e4m3 q) or
+ *                        IDX_NVFP4 (with bf16 q); other pairs: IDX_ERR_UNSUPPORTED
+ *   num_pages:           pages in the pool (page ids outside [0, num_pages) are not
+ *                        read and set IDX_DEVERR_BAD_PAGE)
+ *   page_table (device): int32 [n_slots][max_pages], page of token t of the request
+ *                        in slot s = page_table[s][t / 64]
+ *   slot_ids (device):   int32 [R]; a slot outside [0, n_slots) marks a pad request
+ *                        (graph padding): nothing is read, all its rows are pads
+ *   row_lens (device):   int32 [R][P], tokens of each draft row (its causal length);
+ *                        <= 0 gives an all-pad row; > max_pages*64 is clamped
+ *   init_blocks, local_blocks >= 0 with init_blocks + local_blocks <= topk
+ *   topk:                1 ..IDX_MAX_TOPK
+ *   out_ids (device):    int32 [R][P*G][topk]
+ *   out_scores (device): fp32 [R][P*G][topk]
+ *   workspace (device):  >= idx_score_topk_workspace_bytes(R, P, G, max_pages) bytes,
+ *                        256-byte aligned; overwritten; its first 4 bytes hold the
+ *                        device error flags (IDX_DEVERR_*) of the call.
+ * Output row i of request r: its forced blocks in ascending id order, then the chosen
+ * blocks by descending score (ties to the lower id), then (-1, -inf) pads.  Scores are
+ * raw q.k block maxima (fp8: code dot products times q_scale times the key's scale).
+ * Asynchronous on stream; allocates nothing; capturable in a CUDA graph.
+ * Host-side checks return IDX_ERR_INVALID (P*G outside [1,16], topk out of range,
+ * init+local > topk, NULL pointers, R < 0, n_slots or max_pages < 1, workspace too
+ * small or misaligned, num_pages < 1).  With R == 0 only the workspace is required
+ * (its header is cleared) and the per-request pointers may be NULL.
+ */
+IDX_API int idx_score_topk(const void* q, const float* q_scale, int q_dtype,
+                   const void* k_payload, const void* k_scale, int k_dtype, int64_t num_pages,
+                   const int32_t* page_table, int n_slots, int max_pages,
+                   const int32_t* slot_ids, const int32_t* row_lens,
+                   int num_requests, int packed_queries, int gqa,
+                   int init_blocks, int local_blocks, int topk,
+                   int32_t* out_ids, float* out_scores,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * idx_score_topk_perrow — the same step with every draft row scored as its own decode
+ * row (the per-row kernel the packed one replaces: sglang #45451, Motivation; sglang
+ * #42614, Motivation): the tile holds G live rows and each request's keys are read
+ * once per draft row.  Same arguments, same outputs, same workspace size; an internal
+ * ablation of the packed kernel.
+ */
+IDX_API int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dtype,
+                          const void* k_payload, const void* k_scale, int k_dtype,
+                          int64_t num_pages, const int32_t* page_table, int n_slots,
+                          int max_pages, const int32_t* slot_ids, const int32_t* row_lens,
+                          int num_requests, int packed_queries, int gqa,
+                          int init_blocks, int local_blocks, int topk,
+                          int32_t* out_ids, float* out_scores,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* idx_set_kernel_events — instrumentation for timing.  Arms, for the next
+ * idx_score_topk / idx_score_topk_perrow call on the calling host thread only, up
+ * to three cudaEvent_t (passed as void*, NULL to skip) that the call records on its
+ * stream: before the score kernel, after the score kernel, after the top-k kernel.
+ * The events are used once and then forgotten. */
+IDX_API int idx_set_kernel_events(void* score_begin, void* score_end, void* topk_end);
+
+/* idx_set_grid_limit — cap the number of CTAs the score kernel launches (process-
+ * wide; 0 restores the default of one CTA per SM).  Results do not depend on it:
+ * each block max is computed whole by one warp, so any split of the work gives the
+ * same bits.  Meant for tests and tuning. */
+IDX_API int idx_set_grid_limit(int max_ctas);
+
+/* idx_workspace_errors — read the device error flags of the last call that used this
+ * workspace (syncs on stream).  flags (host): receives the IDX_DEVERR_* bits. */
+IDX_API int idx_workspace_errors(const void* workspace, void* stream, uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBIDX_IDX_H_ */

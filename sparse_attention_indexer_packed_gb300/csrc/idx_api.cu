@@ -1,0 +1,346 @@
+// C ABI of libidx: argument checks, tensor-map set-up and kernel launches.
+// Every entry point returns an idx_status; the message of the last failure on
+// the calling host thread is available from idx_last_error().
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+
+#include "../../include/idx.h"
+#include "idx_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local cudaEvent_t g_ev[3] = {nullptr, nullptr, nullptr};
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(IDX_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t payload_row_bytes(int dtype) {
+  switch (dtype) {
+    case IDX_BF16: return 256;
+    case IDX_FP8_E4M3: return 128;
+    case IDX_NVFP4: return 64;
+    default: return -1;
+  }
+}
+
+int64_t scale_row_bytes(int dtype) {
+  switch (dtype) {
+    case IDX_BF16: return 0;
+    case IDX_FP8_E4M3: return 4;
+    case IDX_NVFP4: return 8;
+    default: return -1;
+  }
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime so the library
+// carries no link-time dependency on the driver library.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map over the payload plane, one 64-row (one page) box per load:
+//  bf16: 128 bf16 per row, box 64 x 64 (two boxes per page), 128-byte swizzle
+//  fp8:  128 bytes per row, box 128 x 64, 128-byte swizzle
+//  fp4:  64 bytes per row,  box 64 x 64,  64-byte swizzle
+int make_payload_map(int dtype, const void* payload, int64_t num_pages, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t rows = (cuuint64_t)num_pages * idx::kPage;
+  cuuint64_t dims[2];
+  cuuint64_t strides[1];
+  cuuint32_t box[2];
+  const cuuint32_t estride[2] = {1, 1};
+  CUtensorMapDataType dt;
+  CUtensorMapSwizzle sw;
+  if (dtype == IDX_BF16) {
+    dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    dims[0] = 128; strides[0] = 256; box[0] = 64; sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  } else if (dtype == IDX_FP8_E4M3) {
+    dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    dims[0] = 128; strides[0] = 128; box[0] = 128; sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  } else {
+    dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    dims[0] = 64; strides[0] = 64; box[0] = 64; sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  }
+  dims[1] = rows;
+  box[1] = idx::kPage;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(payload), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return IDX_OK;
+}
+
+int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtype,
+                    const void* k_payload, const void* k_scale, int k_dtype, int64_t num_pages,
+                    const int32_t* page_table, int n_slots, int max_pages, const int32_t* slot_ids,
+                    const int32_t* row_lens, int R, int P, int G, int init_blocks,
+                    int local_blocks, int topk, int32_t* out_ids, float* out_scores,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (R < 0) return fail(IDX_ERR_INVALID, "num_requests must be >= 0 (got %d)", R);
+  if (P < 1 || G < 1 || P * G > IDX_MAX_PACKED_ROWS)
+    return fail(IDX_ERR_INVALID, "packed_queries * gqa must be in [1, 16] (got %d x %d)", P, G);
+  if (topk < 1 || topk > IDX_MAX_TOPK)
+    return fail(IDX_ERR_INVALID, "topk must be in [1, %d] (got %d)", IDX_MAX_TOPK, topk);
+  if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > topk)
+    return fail(IDX_ERR_INVALID,
+                "need init_blocks, local_blocks >= 0 and init + local <= topk (got %d, %d, %d)",
+                init_blocks, local_blocks, topk);
+  const bool pair_ok = (k_dtype == IDX_BF16 && q_dtype == IDX_BF16) ||
+                       (k_dtype == IDX_FP8_E4M3 && q_dtype == IDX_FP8_E4M3) ||
+                       (k_dtype == IDX_NVFP4 && q_dtype == IDX_BF16);
+  if (!pair_ok)
+    return fail(IDX_ERR_UNSUPPORTED, "unsupported (k_dtype, q_dtype) = (%d, %d)", k_dtype, q_dtype);
+  if (n_slots < 1 || max_pages < 1 || max_pages > 65536)
+    return fail(IDX_ERR_INVALID, "need n_slots >= 1 and 1 <= max_pages <= 65536 (got %d, %d)",
+                n_slots, max_pages);
+  if (num_pages < 1 || num_pages * idx::kPage > 0x7fffffffLL)
+    return fail(IDX_ERR_INVALID, "num_pages must be in [1, 2^31 / 64) (got %lld)",
+                (long long)num_pages);
+  if (!workspace) return fail(IDX_ERR_INVALID, "workspace is NULL");
+  if (R > 0 && (!q || !k_payload || !page_table || !slot_ids || !row_lens || !out_ids ||
+                !out_scores))
+    return fail(IDX_ERR_INVALID, "a required pointer is NULL");
+  if (R > 0 && k_dtype != IDX_BF16 && !k_scale) return fail(IDX_ERR_INVALID, "k_scale is NULL");
+  if (R > 0 && q_dtype == IDX_FP8_E4M3 && !q_scale)
+    return fail(IDX_ERR_INVALID, "q_scale is NULL");
+  if (!aligned(k_payload, 16) || (k_scale && !aligned(k_scale, 16)) || !aligned(q, 16))
+    return fail(IDX_ERR_INVALID, "q, k_payload and k_scale must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(IDX_ERR_INVALID, "workspace must be 256-byte aligned");
+  const size_t need = idx_score_topk_workspace_bytes(R, P, G, max_pages);
+  if (workspace_bytes < need)
+    return fail(IDX_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, IDX_WORKSPACE_HEADER_BYTES, st);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+  if (R == 0) return IDX_OK;
+
+  CUtensorMap map;
+  int rc = make_payload_map(k_dtype, k_payload, num_pages, &map);
+  if (rc != IDX_OK) return rc;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  idx::ScoreArgs sa;
+  sa.q = static_cast<const uint8_t*>(q);
+  sa.q_scale = q_scale;
+  sa.k_scale = static_cast<const uint8_t*>(k_scale);
+  sa.page_table = page_table;
+  sa.slot_ids = slot_ids;
+  sa.row_lens = row_lens;
+  sa.blockmax = reinterpret_cast<float*>(ws + IDX_WORKSPACE_HEADER_BYTES);
+  sa.err = reinterpret_cast<uint32_t*>(ws);
+  sa.num_pages = num_pages;
+  sa.n_slots = n_slots;
+  sa.max_pages = max_pages;
+  sa.nb_cap = (max_pages + 1) / 2;
+  sa.R = R;
+  sa.P = P;
+  sa.G = G;
+  sa.M = P * G;
+  sa.perrow = perrow ? 1 : 0;
+  cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
+  g_ev[0] = g_ev[1] = g_ev[2] = nullptr;
+  if (ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
+  e = idx::launch_score(k_dtype, sa, map, st);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
+  if (ev[1] && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
+
+  idx::TopkArgs ta;
+  ta.blockmax = sa.blockmax;
+  ta.slot_ids = slot_ids;
+  ta.row_lens = row_lens;
+  ta.out_ids = out_ids;
+  ta.out_scores = out_scores;
+  ta.err = sa.err;
+  ta.n_slots = n_slots;
+  ta.max_pages = max_pages;
+  ta.nb_cap = sa.nb_cap;
+  ta.R = R;
+  ta.P = P;
+  ta.G = G;
+  ta.M = P * G;
+  ta.init_blocks = init_blocks;
+  ta.local_blocks = local_blocks;
+  ta.topk = topk;
+  e = idx::launch_topk(ta, st);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the top-k kernel");
+  if (ev[2] && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
+  return IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int idx_abi_version(void) { return IDX_ABI_VERSION; }
+
+const char* idx_status_string(int status) {
+  switch (status) {
+    case IDX_OK: return "IDX_OK";
+    case IDX_ERR_INVALID: return "IDX_ERR_INVALID";
+    case IDX_ERR_UNSUPPORTED: return "IDX_ERR_UNSUPPORTED";
+    case IDX_ERR_CUDA: return "IDX_ERR_CUDA";
+    case IDX_ERR_OOM: return "IDX_ERR_OOM";
+    default: return "IDX_ERR_UNKNOWN";
+  }
+}
+
+const char* idx_last_error(void) { return g_last_error.c_str(); }
+
+int idx_pool_alloc(int dtype, int64_t num_pages, int page_size, int dim, idx_pool* out) {
+  if (!out) return fail(IDX_ERR_INVALID, "out is NULL");
+  if (payload_row_bytes(dtype) < 0) return fail(IDX_ERR_INVALID, "unknown dtype %d", dtype);
+  if (page_size != IDX_PAGE_SIZE || dim != IDX_DIM)
+    return fail(IDX_ERR_INVALID, "page_size must be 64 and dim 128 (got %d, %d)", page_size, dim);
+  if (num_pages < 1 || num_pages * idx::kPage > 0x7fffffffLL)
+    return fail(IDX_ERR_INVALID, "num_pages must be in [1, 2^31 / 64) (got %lld)",
+                (long long)num_pages);
+  memset(out, 0, sizeof(*out));
+  const int64_t rows = num_pages * IDX_PAGE_SIZE;
+  void* payload = nullptr;
+  void* scale = nullptr;
+  cudaError_t e = cudaMalloc(&payload, (size_t)(rows * payload_row_bytes(dtype)));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_OOM, "cudaMalloc of the payload plane failed: %s", cudaGetErrorString(e));
+  }
+  if (scale_row_bytes(dtype) > 0) {
+    e = cudaMalloc(&scale, (size_t)(rows * scale_row_bytes(dtype)));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(payload);
+      return fail(IDX_ERR_OOM, "cudaMalloc of the scale plane failed: %s", cudaGetErrorString(e));
+    }
+  }
+  out->dtype = dtype;
+  out->page_size = page_size;
+  out->dim = dim;
+  out->num_pages = num_pages;
+  out->payload = payload;
+  out->scale = scale;
+  out->payload_row_bytes = payload_row_bytes(dtype);
+  out->scale_row_bytes = scale_row_bytes(dtype);
+  return IDX_OK;
+}
+
+int idx_pool_free(idx_pool* pool) {
+  if (!pool) return fail(IDX_ERR_INVALID, "pool is NULL");
+  cudaError_t e1 = pool->payload ? cudaFree(pool->payload) : cudaSuccess;
+  cudaError_t e2 = pool->scale ? cudaFree(pool->scale) : cudaSuccess;
+  memset(pool, 0, sizeof(*pool));
+  if (e1 != cudaSuccess) return cuda_fail(e1, "cudaFree of the payload plane");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFree of the scale plane");
+  return IDX_OK;
+}
+
+int idx_store_nvfp4(const void* src_bf16, const int64_t* slot_mapping, int64_t num_tokens,
+                    const idx_pool* pool, void* stream) {
+  if (!pool) return fail(IDX_ERR_INVALID, "pool is NULL");
+  if (pool->dtype != IDX_NVFP4 || pool->payload_row_bytes != 64 || pool->scale_row_bytes != 8 ||
+      pool->page_size != IDX_PAGE_SIZE || pool->dim != IDX_DIM)
+    return fail(IDX_ERR_INVALID, "pool is not an NVFP4 pool with 64-token pages of dim 128");
+  if (num_tokens < 0) return fail(IDX_ERR_INVALID, "num_tokens must be >= 0");
+  if (num_tokens == 0) return IDX_OK;
+  if (!src_bf16 || !slot_mapping || !pool->payload || !pool->scale)
+    return fail(IDX_ERR_INVALID, "a required pointer is NULL");
+  if (!aligned(src_bf16, 16) || !aligned(pool->payload, 8))
+    return fail(IDX_ERR_INVALID, "src_bf16 must be 16-byte and the payload 8-byte aligned");
+  if (num_tokens > (int64_t)0x7fffffff * 32)
+    return fail(IDX_ERR_INVALID, "num_tokens too large");
+  cudaError_t e = idx::launch_store_nvfp4(
+      static_cast<const uint16_t*>(src_bf16), slot_mapping, num_tokens,
+      static_cast<uint8_t*>(pool->payload), static_cast<uint8_t*>(pool->scale),
+      pool->num_pages * IDX_PAGE_SIZE, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the NVFP4 store kernel");
+  return IDX_OK;
+}
+
+size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queries, int gqa,
+                                      int max_pages) {
+  if (num_requests < 0 || packed_queries < 1 || gqa < 1 || max_pages < 1) return 0;
+  const size_t nb_cap = (size_t)(max_pages + 1) / 2;
+  return IDX_WORKSPACE_HEADER_BYTES +
+         (size_t)num_requests * packed_queries * gqa * nb_cap * sizeof(float);
+}
+
+int idx_score_topk(const void* q, const float* q_scale, int q_dtype, const void* k_payload,
+                   const void* k_scale, int k_dtype, int64_t num_pages, const int32_t* page_table,
+                   int n_slots, int max_pages, const int32_t* slot_ids, const int32_t* row_lens,
+                   int num_requests, int packed_queries, int gqa, int init_blocks,
+                   int local_blocks, int topk, int32_t* out_ids, float* out_scores,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  return score_topk_impl(false, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
+                         page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
+                         packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
+                         out_scores, workspace, workspace_bytes, stream);
+}
+
+int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dtype, const void* k_payload,
+                          const void* k_scale, int k_dtype, int64_t num_pages,
+                          const int32_t* page_table, int n_slots, int max_pages,
+                          const int32_t* slot_ids, const int32_t* row_lens, int num_requests,
+                          int packed_queries, int gqa, int init_blocks, int local_blocks,
+                          int topk, int32_t* out_ids, float* out_scores, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return score_topk_impl(true, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
+                         page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
+                         packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
+                         out_scores, workspace, workspace_bytes, stream);
+}
+
+int idx_set_grid_limit(int max_ctas) {
+  if (max_ctas < 0) return fail(IDX_ERR_INVALID, "max_ctas must be >= 0");
+  idx::set_grid_limit(max_ctas);
+  return IDX_OK;
+}
+
+int idx_set_kernel_events(void* score_begin, void* score_end, void* topk_end) {
+  g_ev[0] = static_cast<cudaEvent_t>(score_begin);
+  g_ev[1] = static_cast<cudaEvent_t>(score_end);
+  g_ev[2] = static_cast<cudaEvent_t>(topk_end);
+  return IDX_OK;
+}
+
+int idx_workspace_errors(const void* workspace, void* stream, uint32_t* flags) {
+  if (!workspace || !flags) return fail(IDX_ERR_INVALID, "a required pointer is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace flags");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "synchronising the stream");
+  return IDX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Shared declarations between the kernel translation units and the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace idx {
+
+constexpr int kPage = 64;     // tokens per page
+constexpr int kBlock = 128;   // tokens per scored block
+constexpr int kDim = 128;     // head dim
+constexpr int kTileRows = 16; // packed rows per dot tile
+constexpr int kMaxTopk = 256; // largest topk a call may ask for
+
+// Key formats, matching idx_dtype.
+enum KeyFormat : int { kBf16 = 0, kFp8 = 1, kNvfp4 = 2 };
+
+// Arguments of one scoring pass.  A "group" is the set of tile rows that share
+// one read of the keys: a whole request when packed, one draft row when per-row.
+struct ScoreArgs {
+  const uint8_t* q;            // [R][P][G][128] bf16 or e4m3
+  const float* q_scale;        // [R][P*G] (e4m3 q) or nullptr
+  const uint8_t* k_scale;      // scale plane (fp8: 4 B / key, NVFP4: 8 B / key)
+  const int32_t* page_table;   // [n_slots][max_pages]
+  const int32_t* slot_ids;     // [R]
+  const int32_t* row_lens;     // [R][P]
+  float* blockmax;             // [R*P*G][nb_cap]
+  uint32_t* err;               // device error flags
+  int64_t num_pages;
+  int n_slots, max_pages, nb_cap;
+  int R, P, G, M;
+  int perrow;                  // 0: groups are requests; 1: groups are draft rows
+};
+
+struct TopkArgs {
+  const float* blockmax;       // [R*M][nb_cap]
+  const int32_t* slot_ids;
+  const int32_t* row_lens;
+  int32_t* out_ids;            // [R*M][topk]
+  float* out_scores;
+  uint32_t* err;
+  int n_slots, max_pages, nb_cap;
+  int R, P, G, M;
+  int init_blocks, local_blocks, topk;
+};
+
+// Process-wide cap on the score kernel's grid (0 = one CTA per SM).
+void set_grid_limit(int max_ctas);
+int grid_limit();
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_score(int key_format, const ScoreArgs& args, const CUtensorMap& payload_map,
+                         cudaStream_t stream);
+cudaError_t launch_topk(const TopkArgs& args, cudaStream_t stream);
+cudaError_t launch_store_nvfp4(const uint16_t* src, const int64_t* slot_mapping, int64_t num_tokens,
+                               uint8_t* payload, uint8_t* scale, int64_t num_rows,
+                               cudaStream_t stream);
+
+}  // namespace idx

@@ -1,0 +1,641 @@
+// Packed index-score kernel: per-row masked q.k and per-128-token block max.
+//
+// What it computes (sglang #45451, Modifications; sglang #42614 "[AMD]
+// MiniMax-M3 indexer CP: packed scoring for EAGLE verify rows", Modifications 1):
+// the P draft rows x G heads of a request (P*G <= 16) share one 16-row dot tile,
+// so each key tile crosses HBM once per request; tile row i is (draft row i / G,
+// head i % G); the keys are read up to the group's longest row while each row
+// masks tokens at or past its own length; each row emits the max score of every
+// 128-token block it covers.
+//
+// How (sm_103a):
+//  * persistent grid, one CTA per SM; the flattened (group, block) work list is
+//    split into equal contiguous ranges, one per CTA;
+//  * warp 0 produces: it resolves pages through the slot table (a warp-wide
+//    gather for 32 blocks at a time) and issues TMA tensor loads of the 64-token
+//    pages into a ring of shared-memory stages (128-byte or 64-byte swizzle),
+//    plus 1-D bulk copies of the per-key scales, each stage completing on an
+//    mbarrier;
+//  * consumer warps each take whole 128-token blocks: ldmatrix from the swizzled
+//    stage, mma.sync with the query tile held in registers (bf16 m16n8k16, e4m3
+//    m16n8k32; NVFP4 keys are decoded to exact f16 in registers and use f16
+//    m16n8k16), masks by each row's length and reduces the block max with
+//    shuffles;
+//  * every wait is bounded: on timeout the CTA records IDX_DEVERR_TIMEOUT and
+//    winds down after its copies in flight have landed.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "idx_internal.cuh"
+#include "idx_ptx.cuh"
+
+namespace idx {
+
+namespace {
+
+constexpr uint32_t kErrBadPage = 1u;
+constexpr uint32_t kErrTimeout = 2u;
+
+template <int KF>
+struct Cfg;
+
+template <>
+struct Cfg<kBf16> {
+  static constexpr int kRowBytes = 256;
+  static constexpr int kPagePayload = kPage * kRowBytes;  // 16 KB: two 8 KB swizzled boxes
+  static constexpr int kScaleRow = 0;
+  static constexpr int kStages = 6;
+  static constexpr int kConsumers = 6;
+};
+template <>
+struct Cfg<kFp8> {
+  static constexpr int kRowBytes = 128;
+  static constexpr int kPagePayload = kPage * kRowBytes;  // 8 KB: one swizzled box
+  static constexpr int kScaleRow = 4;
+  static constexpr int kStages = 12;
+  static constexpr int kConsumers = 4;
+};
+template <>
+struct Cfg<kNvfp4> {
+  static constexpr int kRowBytes = 64;
+  static constexpr int kPagePayload = kPage * kRowBytes;  // 4 KB: one 64B-swizzled box
+  static constexpr int kScaleRow = 8;
+  static constexpr int kStages = 24;
+  static constexpr int kConsumers = 8;
+};
+
+// Unit k of a CTA goes to stage k % S and consumer warp k % NC.  S is a multiple
+// of NC, so each stage is only ever read by one warp, which therefore waits on
+// its stage's phases strictly in order: a parity wait can never be satisfied by
+// the phase before the one it means.
+template <int KF>
+struct Layout {
+  static_assert(Cfg<KF>::kStages % Cfg<KF>::kConsumers == 0, "stages must split evenly");
+  static constexpr int kStagePayload = 2 * Cfg<KF>::kPagePayload;
+  static constexpr int kPageScale = kPage * Cfg<KF>::kScaleRow;
+  static constexpr int kStageScale = 2 * kPageScale;
+  static constexpr int S = Cfg<KF>::kStages;
+  static constexpr int kPayloadOff = 0;
+  static constexpr int kScaleOff = kPayloadOff + S * kStagePayload;
+  static constexpr int kBarOff = kScaleOff + S * kStageScale;        // full[S], empty[S]
+  static constexpr int kMetaOff = kBarOff + 2 * S * 8;               // int2 per stage
+  static constexpr int kCtlOff = kMetaOff + S * 8;                   // control words
+  static constexpr int kBytes = kCtlOff + 64;
+  static constexpr int kSmemBytes = kBytes + 1024;                   // + alignment slack
+  static constexpr int kThreads = 32 * (1 + Cfg<KF>::kConsumers);
+};
+
+struct Group {
+  int r, slot, base_row, nrows, extent, nbk;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int max_tokens) {
+  return L > max_tokens ? max_tokens : L;
+}
+
+// Geometry of scoring group v (a request when packed, a draft row when per-row).
+__device__ Group group_info(const ScoreArgs& a, int v) {
+  Group g;
+  int ext = 0;
+  if (a.perrow) {
+    g.r = v / a.P;
+    const int j = v - g.r * a.P;
+    g.base_row = g.r * a.M + j * a.G;
+    g.nrows = a.G;
+    ext = __ldg(a.row_lens + v);
+  } else {
+    g.r = v;
+    g.base_row = v * a.M;
+    g.nrows = a.M;
+    for (int j = 0; j < a.P; ++j) ext = max(ext, __ldg(a.row_lens + v * a.P + j));
+  }
+  g.slot = __ldg(a.slot_ids + g.r);
+  const bool pad = g.slot < 0 || g.slot >= a.n_slots;
+  ext = clamp_len(ext, a.max_pages * kPage);
+  g.extent = pad ? 0 : max(ext, 0);
+  g.nbk = (g.extent + kBlock - 1) / kBlock;
+  return g;
+}
+
+// Length of tile row i of group v (clamped; <= 0 means the row is empty).
+__device__ __forceinline__ int tile_row_len(const ScoreArgs& a, int v, int r, int i) {
+  const int L = a.perrow ? __ldg(a.row_lens + v) : __ldg(a.row_lens + r * a.P + i / a.G);
+  return clamp_len(L, a.max_pages * kPage);
+}
+
+__device__ __forceinline__ float fmax_nan_free(float a, float b) { return a > b ? a : b; }
+
+// ---------------------------------------------------------------------------
+// Query tiles in mma.sync A-fragment order.
+// ---------------------------------------------------------------------------
+template <int KF>
+struct QTile;
+
+// bf16: 8 k-steps of 16, a[ks] = {A[g][16ks+2t..], A[g+8][..], A[g][16ks+8+2t..], A[g+8][..]}
+template <>
+struct QTile<kBf16> {
+  uint32_t a[8][4];
+  __device__ float post_scale() const { return 1.f; }
+  __device__ void load(const ScoreArgs& args, int q_row0, int nrows, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* r0 = args.q + (size_t)(q_row0 + g) * 256;
+    const uint8_t* r1 = args.q + (size_t)(q_row0 + g + 8) * 256;
+    const bool v0 = g < nrows, v1 = g + 8 < nrows;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int o0 = (16 * ks + 2 * t) * 2, o1 = (16 * ks + 8 + 2 * t) * 2;
+      a[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(r0 + o0)) : 0u;
+      a[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(r1 + o0)) : 0u;
+      a[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(r0 + o1)) : 0u;
+      a[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(r1 + o1)) : 0u;
+    }
+  }
+};
+
+// e4m3: 4 k-steps of 32, a[ks] = {A[g][32ks+4t..+3], A[g+8][..], A[g][32ks+16+4t..], A[g+8][..]}
+template <>
+struct QTile<kFp8> {
+  uint32_t a[4][4];
+  __device__ float post_scale() const { return 1.f; }
+  __device__ void load(const ScoreArgs& args, int q_row0, int nrows, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* r0 = args.q + (size_t)(q_row0 + g) * 128;
+    const uint8_t* r1 = args.q + (size_t)(q_row0 + g + 8) * 128;
+    const bool v0 = g < nrows, v1 = g + 8 < nrows;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int o0 = 32 * ks + 4 * t, o1 = 32 * ks + 16 + 4 * t;
+      a[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(r0 + o0)) : 0u;
+      a[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(r1 + o0)) : 0u;
+      a[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(r0 + o1)) : 0u;
+      a[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(r1 + o1)) : 0u;
+    }
+  }
+};
+
+// NVFP4 keys with bf16 q: the query is rescaled by 2^qexp (one power of two per
+// group, chosen so its largest magnitude lands in [2^14, 2^15)) and stored as
+// f16, exact for every element within 2^24 of the largest.  The decoded keys
+// (e2m1 x E4M3) are exact in f16, so each product is exact and the fp32 sum is
+// rescaled by 2^-qexp afterwards.
+//
+// k order: k-step ks = 2m + hh takes, for thread t, the elements
+// d = 32m + 8t + 4hh + {0,1} (b0) and + {2,3} (b1) of its key, which is the order
+// the packed bytes of the key arrive in; the query is gathered the same way.
+template <>
+struct QTile<kNvfp4> {
+  uint32_t a[8][4];
+  float inv_scale;  // 2^-qexp
+  __device__ float post_scale() const { return inv_scale; }
+  __device__ void load(const ScoreArgs& args, int q_row0, int nrows, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const bool v0 = g < nrows, v1 = g + 8 < nrows;
+    const __nv_bfloat16* r0 = reinterpret_cast<const __nv_bfloat16*>(args.q) + (size_t)(q_row0 + g) * 128;
+    const __nv_bfloat16* r1 = reinterpret_cast<const __nv_bfloat16*>(args.q) + (size_t)(q_row0 + g + 8) * 128;
+    float x0[4][8], x1[4][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      uint4 u0 = v0 ? __ldg(reinterpret_cast<const uint4*>(r0 + 32 * m + 8 * t)) : make_uint4(0, 0, 0, 0);
+      uint4 u1 = v1 ? __ldg(reinterpret_cast<const uint4*>(r1 + 32 * m + 8 * t)) : make_uint4(0, 0, 0, 0);
+      const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w};
+      const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x0[m][2 * e] = __uint_as_float(w0[e] << 16);
+        x0[m][2 * e + 1] = __uint_as_float(w0[e] & 0xffff0000u);
+        x1[m][2 * e] = __uint_as_float(w1[e] << 16);
+        x1[m][2 * e + 1] = __uint_as_float(w1[e] & 0xffff0000u);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(x0[m][e]), fabsf(x1[m][e])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int qexp = 0;
+    if (amax > 0.f) {
+      const int e = ((__float_as_uint(amax) >> 23) & 0xff) - 127;  // amax in [2^e, 2^(e+1))
+      qexp = 14 - e;
+    }
+    qexp = max(-100, min(100, qexp));
+    const float up = ldexpf(1.f, qexp);
+    inv_scale = ldexpf(1.f, -qexp);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int ks = 2 * m + hh;
+        const float* p0 = &x0[m][4 * hh];
+        const float* p1 = &x1[m][4 * hh];
+        __half2 h;
+        h = __floats2half2_rn(p0[0] * up, p0[1] * up);
+        a[ks][0] = *reinterpret_cast<uint32_t*>(&h);
+        h = __floats2half2_rn(p1[0] * up, p1[1] * up);
+        a[ks][1] = *reinterpret_cast<uint32_t*>(&h);
+        h = __floats2half2_rn(p0[2] * up, p0[3] * up);
+        a[ks][2] = *reinterpret_cast<uint32_t*>(&h);
+        h = __floats2half2_rn(p1[2] * up, p1[3] * up);
+        a[ks][3] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Block max of one 128-token block for the 16 tile rows (one warp).
+// Returns the running maxima of rows g (mx0) and g + 8 (mx1) over the tokens
+// this lane saw; the caller reduces across the 4 lanes of a row.
+// ---------------------------------------------------------------------------
+template <int KF>
+struct BlockScorer;
+
+template <>
+struct BlockScorer<kBf16> {
+  __device__ static void run(const QTile<kBf16>& qt, uint32_t stage, uint32_t /*scale_stage*/,
+                             const float* /*scale_smem*/, int lane, int tbase, int L0, int L1,
+                             float qs0, float qs1, float& mx0, float& mx1) {
+    const int t = lane & 3;
+    const int m = lane >> 3, rr = lane & 7;
+#pragma unroll 2
+    for (int nt = 0; nt < 16; ++nt) {
+      const int j = nt * 8 + rr;
+      const int p = j >> 6, n = j & 63;
+      const uint32_t row_base = stage + (uint32_t)(p * 8192 + n * 128);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int qd = 4 * c + m;  // 16-byte chunk of d (0..15)
+        const int h = qd >> 3, cq = qd & 7;
+        const uint32_t addr = row_base + (uint32_t)(h * 16384) + (uint32_t)(((cq ^ rr) & 7) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(addr, b0, b1, b2, b3);
+        mma_bf16_16816(acc, qt.a[2 * c], b0, b1);
+        mma_bf16_16816(acc, qt.a[2 * c + 1], b2, b3);
+      }
+      const int t0 = tbase + nt * 8 + 2 * t;
+      if (t0 < L0) mx0 = fmax_nan_free(mx0, acc[0]);
+      if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, acc[1]);
+      if (t0 < L1) mx1 = fmax_nan_free(mx1, acc[2]);
+      if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, acc[3]);
+    }
+    (void)qs0;
+    (void)qs1;
+  }
+};
+
+template <>
+struct BlockScorer<kFp8> {
+  __device__ static void run(const QTile<kFp8>& qt, uint32_t stage, uint32_t /*scale_stage*/,
+                             const float* scale_smem, int lane, int tbase, int L0, int L1,
+                             float qs0, float qs1, float& mx0, float& mx1) {
+    const int t = lane & 3;
+    const int m = lane >> 3, rr = lane & 7;
+#pragma unroll 2
+    for (int nt = 0; nt < 16; ++nt) {
+      const int j = nt * 8 + rr;
+      const int p = j >> 6, n = j & 63;
+      const uint32_t row_base = stage + (uint32_t)(p * 8192 + n * 128);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int qd = 4 * c + m;  // 16-byte chunk of the 128-byte row
+        const uint32_t addr = row_base + (uint32_t)(((qd ^ rr) & 7) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(addr, b0, b1, b2, b3);
+        mma_e4m3_16832(acc, qt.a[2 * c], b0, b1);
+        mma_e4m3_16832(acc, qt.a[2 * c + 1], b2, b3);
+      }
+      const int jt = nt * 8 + 2 * t;  // token of acc[0] within the block
+      const float2 ks = *reinterpret_cast<const float2*>(scale_smem + jt);
+      const int t0 = tbase + jt;
+      if (t0 < L0) mx0 = fmax_nan_free(mx0, (acc[0] * qs0) * ks.x);
+      if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, (acc[1] * qs0) * ks.y);
+      if (t0 < L1) mx1 = fmax_nan_free(mx1, (acc[2] * qs1) * ks.x);
+      if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, (acc[3] * qs1) * ks.y);
+    }
+  }
+};
+
+template <>
+struct BlockScorer<kNvfp4> {
+  __device__ static void run(const QTile<kNvfp4>& qt, uint32_t stage, uint32_t scale_stage,
+                             const float* /*scale_smem*/, int lane, int tbase, int L0, int L1,
+                             float /*qs0*/, float /*qs1*/, float& mx0, float& mx1) {
+    const int g = lane >> 2, t = lane & 3;
+    const int m = lane >> 3, rr = lane & 7;
+    const uint32_t th = (uint32_t)(t >> 1);
+    // byte selectors {th, th, 2+th, 2+th}: duplicate the scale of group 2m + th
+    const uint32_t sel = th | (th << 4) | ((2 + th) << 8) | ((2 + th) << 12);
+#pragma unroll 2
+    for (int nt = 0; nt < 16; ++nt) {
+      // B operand: this lane's ldmatrix row address (token nt*8 + rr, chunk m)
+      const int j = nt * 8 + rr;
+      const int p = j >> 6, n = j & 63;
+      const uint32_t addr = stage + (uint32_t)(p * 4096 + n * 64) +
+                            (uint32_t)(((m ^ ((n >> 1) & 3)) & 3) << 4);
+      uint32_t w[4];
+      ldmatrix_x4(addr, w[0], w[1], w[2], w[3]);
+      // scales of the token this lane holds in the B fragment: token nt*8 + g
+      const int jb = nt * 8 + g;
+      const int pb = jb >> 6, nb = jb & 63;
+      uint32_t s_lo, s_hi;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                   : "=r"(s_lo), "=r"(s_hi)
+                   : "r"(scale_stage + (uint32_t)(pb * 512 + nb * 8)));
+      uint32_t sc[4];
+      e4m3x4_to_f16x2x2(prmt(s_lo, 0u, sel), sc[0], sc[1]);
+      e4m3x4_to_f16x2x2(prmt(s_hi, 0u, sel), sc[2], sc[3]);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {
+        uint32_t f[4];
+        e2m1x8_to_f16x2x4(w[mm], f);
+        const uint32_t k0 = hmul2_f16(f[0], sc[mm]);
+        const uint32_t k1 = hmul2_f16(f[1], sc[mm]);
+        const uint32_t k2 = hmul2_f16(f[2], sc[mm]);
+        const uint32_t k3 = hmul2_f16(f[3], sc[mm]);
+        mma_f16_16816(acc, qt.a[2 * mm], k0, k1);
+        mma_f16_16816(acc, qt.a[2 * mm + 1], k2, k3);
+      }
+      const int t0 = tbase + nt * 8 + 2 * t;
+      if (t0 < L0) mx0 = fmax_nan_free(mx0, acc[0]);
+      if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, acc[1]);
+      if (t0 < L1) mx1 = fmax_nan_free(mx1, acc[2]);
+      if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, acc[3]);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <int KF>
+__global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
+    score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap payload_map) {
+  using L = Layout<KF>;
+  using C = Cfg<KF>;
+  constexpr int S = L::S;
+  constexpr int NC = C::kConsumers;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + L::kBarOff;
+  const uint32_t bar_empty = bar_full + S * 8;
+  int2* meta = reinterpret_cast<int2*>(smem + L::kMetaOff);
+  volatile int* ctl = reinterpret_cast<volatile int*>(smem + L::kCtlOff);
+  // ctl[0] = units of this CTA, ctl[1] = first group, ctl[2] = first block, ctl[3] = abort
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + s * 8, 1);
+      mbar_init(bar_empty + s * 8, 1);
+    }
+    fence_barrier_init();
+    prefetch_tensormap(&payload_map);
+  }
+
+  // ---- this CTA's contiguous share of the (group, block) work list ----------
+  const int V = a.perrow ? a.R * a.P : a.R;
+  if (warp == 0) {
+    long long total = 0;
+    for (int v0 = 0; v0 < V; v0 += 32) {
+      const int v = v0 + lane;
+      int nbk = v < V ? group_info(a, v).nbk : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) nbk += __shfl_xor_sync(0xffffffffu, nbk, o);
+      total += nbk;
+    }
+    const long long u0 = total * blockIdx.x / gridDim.x;
+    const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
+    long long prefix = 0;
+    int v_start = V, b_start = 0;
+    for (int v0 = 0; v0 < V && v_start == V; v0 += 32) {
+      const int v = v0 + lane;
+      const int nbk = v < V ? group_info(a, v).nbk : 0;
+      int incl = nbk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const long long excl = prefix + incl - nbk;
+      const bool here = v < V && nbk > 0 && excl <= u0 && u0 < excl + nbk;
+      const unsigned hit = __ballot_sync(0xffffffffu, here);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const long long ex = __shfl_sync(0xffffffffu, excl, src);
+        v_start = v0 + src;
+        b_start = (int)(u0 - ex);
+      }
+      prefix += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      ctl[0] = (int)(u1 - u0);
+      ctl[1] = v_start;
+      ctl[2] = b_start;
+      ctl[3] = 0;
+    }
+  }
+  __syncthreads();
+  const int n_units = ctl[0];
+
+  if (warp == 0) {
+    // ======================= producer =======================================
+    int v = ctl[1], b = ctl[2];
+    Group gi = (n_units > 0) ? group_info(a, v) : Group{};
+    int issued = 0;
+    bool aborted = false;
+    for (int k0 = 0; k0 < n_units && !aborted; k0 += 32) {
+      // lane l describes unit k0 + l
+      int lv = v, lb = b + lane;
+      Group lg = gi;
+      while (lb >= lg.nbk && lv + 1 < V) {
+        lb -= lg.nbk;
+        ++lv;
+        lg = group_info(a, lv);
+      }
+      int p0 = -1, p1 = -1;
+      if (k0 + lane < n_units) {
+        const int32_t* row = a.page_table + (size_t)lg.slot * a.max_pages;
+        p0 = __ldg(row + 2 * lb);
+        const bool two = (lb * kBlock + kPage) < lg.extent;
+        p1 = two ? __ldg(row + 2 * lb + 1) : -1;
+        const bool bad0 = p0 < 0 || p0 >= a.num_pages;
+        const bool bad1 = two && (p1 < 0 || p1 >= a.num_pages);
+        if (bad0 || bad1) atomicOr(a.err, kErrBadPage);
+        if (bad0) p0 = -2;
+        if (bad1) p1 = -2;
+      }
+      // next chunk starts one unit past lane 31's
+      {
+        const int v31 = __shfl_sync(0xffffffffu, lv, 31);
+        const int b31 = __shfl_sync(0xffffffffu, lb, 31);
+        v = v31;
+        b = b31 + 1;
+        gi = group_info(a, v);
+        while (b >= gi.nbk && v < V - 1) {
+          b -= gi.nbk;
+          ++v;
+          gi = group_info(a, v);
+        }
+      }
+      const int cnt = min(32, n_units - k0);
+      for (int u = 0; u < cnt; ++u) {
+        const int uv = __shfl_sync(0xffffffffu, lv, u);
+        const int ub = __shfl_sync(0xffffffffu, lb, u);
+        const int up0 = __shfl_sync(0xffffffffu, p0, u);
+        const int up1 = __shfl_sync(0xffffffffu, p1, u);
+        const int uslot = __shfl_sync(0xffffffffu, lg.slot, u);
+        (void)uslot;
+        if (lane == 0) {
+          const int k = k0 + u;
+          const int s = k % S;
+          if (k >= S) {
+            if (!mbar_wait_bounded(bar_empty + s * 8, ((k / S) - 1) & 1)) {
+              atomicOr(a.err, kErrTimeout);
+              ctl[3] = 1;
+              aborted = true;
+            }
+          }
+          if (!aborted && ctl[3]) aborted = true;
+          if (!aborted) {
+            meta[s] = make_int2(uv, ub);
+            uint32_t tx = 0;
+            if (up0 >= 0) tx += C::kPagePayload + L::kPageScale;
+            if (up1 >= 0) tx += C::kPagePayload + L::kPageScale;
+            const uint32_t full = bar_full + s * 8;
+            mbar_arrive_expect_tx(full, tx);
+            const uint32_t dst = sbase + L::kPayloadOff + s * L::kStagePayload;
+            const uint32_t sdst = sbase + L::kScaleOff + s * L::kStageScale;
+            const int pg[2] = {up0, up1};
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+              if (pg[pp] < 0) continue;
+              const int y = pg[pp] * kPage;
+              if (KF == kBf16) {
+                // two 64-column boxes per page: d 0..63 and d 64..127
+                tma_load_2d(dst + pp * 8192, &payload_map, 0, y, full);
+                tma_load_2d(dst + 16384 + pp * 8192, &payload_map, 64, y, full);
+              } else {
+                tma_load_2d(dst + pp * C::kPagePayload, &payload_map, 0, y, full);
+                bulk_load(sdst + pp * L::kPageScale,
+                          a.k_scale + (size_t)pg[pp] * L::kPageScale, L::kPageScale, full);
+              }
+            }
+            issued = k + 1;
+          }
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
+        if (aborted) break;
+      }
+    }
+    // On abort, let the copies already issued land before the CTA exits.
+    if (lane == 0 && aborted) {
+      for (int k = max(0, issued - S); k < issued; ++k)
+        (void)mbar_wait_bounded(bar_full + (k % S) * 8, (k / S) & 1, 200000000ull);
+    }
+  } else {
+    // ======================= consumers ======================================
+    const int cw = warp - 1;
+    const int g = lane >> 2, t = lane & 3;
+    int cur_v = -1;
+    QTile<KF> qt;
+    int L0 = 0, L1 = 0, row0 = -1, row1 = -1;
+    float qs0 = 1.f, qs1 = 1.f;
+    for (int k = cw; k < n_units; k += NC) {
+      const int s = k % S;
+      if (ctl[3]) break;
+      if (!mbar_wait_bounded(bar_full + s * 8, (k / S) & 1)) {
+        if (lane == 0) {
+          atomicOr(a.err, kErrTimeout);
+          ctl[3] = 1;
+        }
+        break;
+      }
+      const int2 mt = meta[s];
+      const int v = mt.x, b = mt.y;
+      if (v != cur_v) {
+        const Group gi = group_info(a, v);
+        qt.load(a, gi.base_row, gi.nrows, lane);
+        L0 = g < gi.nrows ? tile_row_len(a, v, gi.r, g) : 0;
+        L1 = g + 8 < gi.nrows ? tile_row_len(a, v, gi.r, g + 8) : 0;
+        row0 = g < gi.nrows ? gi.base_row + g : -1;
+        row1 = g + 8 < gi.nrows ? gi.base_row + g + 8 : -1;
+        if (KF == kFp8) {
+          qs0 = row0 >= 0 ? __ldg(a.q_scale + row0) : 0.f;
+          qs1 = row1 >= 0 ? __ldg(a.q_scale + row1) : 0.f;
+        }
+        cur_v = v;
+      }
+      const uint32_t stage = sbase + L::kPayloadOff + s * L::kStagePayload;
+      const uint32_t scale_stage = sbase + L::kScaleOff + s * L::kStageScale;
+      const float* scale_smem = reinterpret_cast<const float*>(smem + L::kScaleOff + s * L::kStageScale);
+      const int tbase = b * kBlock;
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      BlockScorer<KF>::run(qt, stage, scale_stage, scale_smem, lane, tbase, L0, L1, qs0, qs1, mx0, mx1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + s * 8);
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        mx0 = fmax_nan_free(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmax_nan_free(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      if (KF == kNvfp4) {
+        mx0 *= qt.post_scale();
+        mx1 *= qt.post_scale();
+      }
+      if (t == 0) {
+        if (row0 >= 0 && tbase < L0) a.blockmax[(size_t)row0 * a.nb_cap + b] = mx0;
+        if (row1 >= 0 && tbase < L1) a.blockmax[(size_t)row1 * a.nb_cap + b] = mx1;
+      }
+    }
+  }
+}
+
+std::atomic<int> g_grid_limit{0};
+
+template <int KF>
+cudaError_t launch_kf(const ScoreArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+  using L = Layout<KF>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(score_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int lim = g_grid_limit.load(std::memory_order_relaxed);
+  const int grid = (lim > 0 && lim < sms) ? lim : sms;
+  score_kernel<KF><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, map);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+void set_grid_limit(int max_ctas) { g_grid_limit.store(max_ctas < 0 ? 0 : max_ctas); }
+int grid_limit() { return g_grid_limit.load(); }
+
+cudaError_t launch_score(int key_format, const ScoreArgs& args, const CUtensorMap& payload_map,
+                         cudaStream_t stream) {
+  switch (key_format) {
+    case kBf16:
+      return launch_kf<kBf16>(args, payload_map, stream);
+    case kFp8:
+      return launch_kf<kFp8>(args, payload_map, stream);
+    case kNvfp4:
+      return launch_kf<kNvfp4>(args, payload_map, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace idx

@@ -12,15 +12,26 @@ def np_bits16(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def oracle_planes(batch):
+def oracle_planes(batch, requests=None):
     """Pool planes as the oracle sees them.  For NVFP4 the oracle quantises the
-    bf16 staging keys itself (never reading bytes the CUDA path wrote)."""
+    bf16 staging keys itself (never reading bytes the CUDA path wrote); with
+    ``requests`` only those requests' keys are quantised."""
     import oracle
     payload = np_u8(batch.payload).copy()
     scale = None if batch.scale is None else np_u8(batch.scale).copy()
     if batch.spec.k_dtype == "nvfp4" and batch.staging is not None and batch.staging.numel():
-        pay, sc = oracle.formats.nvfp4_quantize(np_bits16(batch.staging))
-        rows = batch.slot_mapping.numpy()
+        if requests is None:
+            sel = slice(None)
+            stage = batch.staging
+            rows = batch.slot_mapping.numpy()
+        else:
+            lens = batch.group_lens()
+            idx = [np.arange(batch.staging_offsets[r], batch.staging_offsets[r] + lens[r])
+                   for r in requests if batch.staging_offsets[r] >= 0]
+            sel = np.concatenate(idx) if idx else np.zeros(0, np.int64)
+            stage = batch.staging[torch.from_numpy(sel)]
+            rows = batch.slot_mapping.numpy()[sel]
+        pay, sc = oracle.formats.nvfp4_quantize(np_bits16(stage))
         keep = rows >= 0
         payload[rows[keep]] = pay[keep]
         scale[rows[keep]] = sc[keep]

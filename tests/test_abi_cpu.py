@@ -1,0 +1,112 @@
+"""The C ABI library loads without a GPU, exports every symbol include/idx.h
+declares, and rejects bad arguments on the host (no compute call runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_indexer_packed_gb300 as idx
+from sparse_attention_indexer_packed_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "idx.h")).read()
+    return sorted(set(re.findall(r"IDX_API\s+[\w\s\*]+?\b(idx_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    return idx.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert "idx_score_topk" in names and "idx_store_nvfp4" in names and "idx_pool_alloc" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib._SIGNATURES), set(names) ^ set(_lib._SIGNATURES)
+
+
+def test_version_and_status_strings(L):
+    assert idx.abi_version() == 1
+    assert L.idx_status_string(0) == b"IDX_OK"
+    assert L.idx_status_string(-1) == b"IDX_ERR_INVALID"
+    assert L.idx_status_string(-2) == b"IDX_ERR_UNSUPPORTED"
+
+
+def test_workspace_bytes(L):
+    assert idx.idx_score_topk_workspace_bytes(16, 4, 4, 2048) == 256 + 16 * 16 * 1024 * 4
+    assert idx.idx_score_topk_workspace_bytes(1, 1, 1, 3) == 256 + 2 * 4
+    assert idx.idx_score_topk_workspace_bytes(0, 4, 4, 10) == 256
+
+
+FAKE = 0x10000  # a non-NULL, 256-aligned value; every case below fails validation first
+
+
+def _call(L, **over):
+    a = dict(q=FAKE, q_scale=None, q_dtype=0, k_payload=FAKE, k_scale=None, k_dtype=0,
+             num_pages=100, page_table=FAKE, n_slots=4, max_pages=8, slot_ids=FAKE,
+             row_lens=FAKE, R=2, P=4, G=4, init=1, local=2, topk=8, out_ids=FAKE,
+             out_scores=FAKE, ws=FAKE, ws_bytes=1 << 20, stream=None)
+    a.update(over)
+    return L.idx_score_topk(a["q"], a["q_scale"], a["q_dtype"], a["k_payload"], a["k_scale"],
+                            a["k_dtype"], a["num_pages"], a["page_table"], a["n_slots"],
+                            a["max_pages"], a["slot_ids"], a["row_lens"], a["R"], a["P"], a["G"],
+                            a["init"], a["local"], a["topk"], a["out_ids"], a["out_scores"],
+                            a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(P=5, G=4), -1),                 # more than 16 packed rows
+    (dict(P=0), -1),
+    (dict(topk=0), -1),
+    (dict(topk=257), -1),
+    (dict(init=4, local=5, topk=8), -1),  # forced blocks cannot fit
+    (dict(local=-1), -1),
+    (dict(R=-1), -1),
+    (dict(q=None), -1),
+    (dict(ws=None), -1),
+    (dict(ws=FAKE + 16), -1),             # misaligned workspace
+    (dict(ws_bytes=100), -1),             # workspace too small
+    (dict(k_dtype=1, q_dtype=0), -2),     # fp8 keys with bf16 q
+    (dict(k_dtype=2, q_dtype=1), -2),     # NVFP4 keys with fp8 q
+    (dict(k_dtype=1, q_dtype=1, k_scale=FAKE), -1),  # fp8 q without q_scale
+    (dict(k_dtype=1, q_dtype=1, q_scale=FAKE), -1),  # fp8 keys without k_scale
+    (dict(n_slots=0), -1),
+    (dict(max_pages=0), -1),
+    (dict(num_pages=0), -1),
+])
+def test_host_side_validation(L, over, status):
+    assert _call(L, **over) == status
+    assert L.idx_last_error() != b""
+
+
+def test_pool_alloc_validation(L):
+    p = _lib.IdxPool()
+    assert L.idx_pool_alloc(0, 10, 32, 128, ctypes.byref(p)) == -1
+    assert L.idx_pool_alloc(0, 10, 64, 64, ctypes.byref(p)) == -1
+    assert L.idx_pool_alloc(7, 10, 64, 128, ctypes.byref(p)) == -1
+    assert L.idx_pool_alloc(0, 0, 64, 128, ctypes.byref(p)) == -1
+
+
+def test_store_validation(L):
+    p = _lib.IdxPool()
+    p.dtype, p.page_size, p.dim, p.num_pages = 0, 64, 128, 10   # not NVFP4
+    p.payload, p.scale, p.payload_row_bytes, p.scale_row_bytes = FAKE, FAKE, 256, 0
+    assert L.idx_store_nvfp4(FAKE, FAKE, 10, ctypes.byref(p), None) == -1
+    p.dtype, p.payload_row_bytes, p.scale_row_bytes = 2, 64, 8
+    assert L.idx_store_nvfp4(FAKE, FAKE, -1, ctypes.byref(p), None) == -1
+    assert L.idx_store_nvfp4(FAKE, FAKE, 0, ctypes.byref(p), None) == 0   # no-op
+
+
+def test_cpu_tensors_are_refused():
+    import torch
+    with pytest.raises(idx.IdxError):
+        idx.idx_store_nvfp4(torch.zeros((1, 128), dtype=torch.bfloat16),
+                            torch.zeros(1, dtype=torch.int64),
+                            (torch.zeros((64, 64), dtype=torch.uint8), torch.zeros((64, 8), dtype=torch.uint8)))

@@ -1,0 +1,263 @@
+"""CUDA path vs the fp64 oracle on the same seeded inputs (needs a GPU).
+
+Bar: NVFP4 stored bytes bit-exact; block-max scores within 1e-3 * (1 + |s|);
+top-k id sets exact except where the oracle's last chosen and best unchosen
+candidates lie within that tolerance (tests/_util.compare_row).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from _util import compare_row, oracle_kwargs, oracle_planes, np_u8, score_tol
+import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_all_rows(batch, out, ref, init_blocks=None, local_blocks=None):
+    s = batch.spec
+    init_blocks = s.init_blocks if init_blocks is None else init_blocks
+    local_blocks = s.local_blocks if local_blocks is None else local_blocks
+    bad = []
+    for r in range(batch.R):
+        for i in range(batch.M):
+            bm = ref.blockmax.get((r, i), np.zeros(0))
+            err = compare_row(out.ids[r, i], out.scores[r, i], ref.ids[r, i], ref.scores[r, i],
+                              bm, init_blocks, local_blocks)
+            if err:
+                bad.append(f"request {r} row {i}: {err}")
+    assert not bad, "\n".join(bad[:20]) + f"\n({len(bad)} rows differ)"
+
+
+def _check_blockmax(batch, out, ref):
+    """Every block max the oracle defines, against the workspace."""
+    worst = 0.0
+    for (r, i), bm in ref.blockmax.items():
+        got = out.blockmax[r * batch.M + i, :len(bm)].astype(np.float64)
+        err = np.abs(got - bm) / score_tol(bm)
+        worst = max(worst, float(err.max()))
+    assert worst <= 1.0, f"block max off by {worst:.3f} x tolerance"
+
+
+TINY_BF16 = workloads.WORKLOADS["tiny_bf16_1x4k"]
+
+
+def test_tiny_bf16():
+    b = workloads.make_batch(TINY_BF16)
+    out = _gpu.run(b)
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    assert out.flags == 0
+    _check_blockmax(b, out, ref)
+    _check_all_rows(b, out, ref)
+
+
+SMALL = []
+for k_dtype, q_dtype in [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3"), ("nvfp4", "bf16")]:
+    for seed, (P, G), lens, pads, init, local, topk in [
+        (101, (4, 4), (1, 9000), (), 1, 2, 16),
+        (102, (4, 4), (1, 3000), (1, 3), 1, 4, 64),
+        (103, (1, 16), (100, 6000), (), 2, 2, 8),
+        (104, (16, 1), (1, 5000), (0,), 0, 0, 5),
+        (105, (2, 3), (1, 4000), (), 1, 0, 12),
+        (106, (4, 4), (120, 700), (), 1, 4, 64),      # nb < topk for most rows
+    ]:
+        SMALL.append(pytest.param(k_dtype, q_dtype, seed, P, G, lens, pads, init, local, topk,
+                                  id=f"{k_dtype}-{seed}-P{P}G{G}"))
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype,seed,P,G,lens,pads,init,local,topk", SMALL)
+def test_small_parity(k_dtype, q_dtype, seed, P, G, lens, pads, init, local, topk):
+    spec = workloads.small_spec(f"s{seed}", seed, k_dtype, q_dtype, R=6, P=P, G=G,
+                                init_blocks=init, local_blocks=local, topk=topk, len_range=lens,
+                                pad_requests=pads)
+    b = workloads.make_batch(spec)
+    out = _gpu.run(b)
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    assert out.flags == 0
+    _check_blockmax(b, out, ref)
+    _check_all_rows(b, out, ref)
+
+
+@pytest.mark.parametrize("name", ["verify_bf16_4x32k", "verify_fp8_4x32k"])
+def test_verify_rows_4x4_ending_32767(name):
+    """4 requests x 4 draft rows ending at tokens 32767..32770: one tile mixes
+    256- and 257-block rows with different local windows."""
+    b = workloads.make_batch(workloads.WORKLOADS[name])
+    out = _gpu.run(b)
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_blockmax(b, out, ref)
+    _check_all_rows(b, out, ref)
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype", [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3"),
+                                             ("nvfp4", "bf16")])
+def test_packed_equals_perrow_bitwise(k_dtype, q_dtype):
+    """Both variants run the same 16-row MMA, so the max scores are equal
+    bit for bit and so are the selections."""
+    spec = workloads.small_spec("pp", 201, k_dtype, q_dtype, R=5, len_range=(1, 7000), topk=32)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    a = _gpu.run(b, planes=planes)
+    p = _gpu.run(b, planes=planes, perrow=True)
+    assert np.array_equal(a.ids, p.ids)
+    assert np.array_equal(a.scores.view(np.uint32), p.scores.view(np.uint32))
+
+
+def test_nvfp4_store_bitexact():
+    spec = workloads.small_spec("st", 301, "nvfp4", "bf16", R=4, len_range=(1, 5000))
+    b = workloads.make_batch(spec)
+    payload, scale = _gpu.device_planes(b)
+    ref_payload, ref_scale = oracle_planes(b)
+    assert np.array_equal(np_u8(payload.cpu()), ref_payload)
+    assert np.array_equal(np_u8(scale.cpu()), ref_scale)
+
+
+def test_nvfp4_store_golden_groups():
+    import test_oracle_formats as F
+    cases = F._read_golden()
+    n = len(cases)
+    src = torch.zeros((n * 8, 128), dtype=torch.bfloat16)
+    for c, (x, sc, pay) in enumerate(cases):
+        for g in range(8):
+            src[c * 8 + g, 16 * g:16 * g + 16] = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+    payload = torch.zeros((n * 8 + 64, 64), dtype=torch.uint8, device="cuda")
+    scale = torch.zeros((n * 8 + 64, 8), dtype=torch.uint8, device="cuda")
+    rows = torch.arange(n * 8, dtype=torch.int64) + 3   # rows shifted off the identity
+    import sparse_attention_indexer_packed_gb300 as idx
+    idx.idx_store_nvfp4(src.cuda(), rows.cuda(), (payload, scale))
+    P = payload.cpu().numpy()
+    S = scale.cpu().numpy()
+    for c, (x, sc, pay) in enumerate(cases):
+        for g in range(8):
+            row = c * 8 + g + 3
+            assert S[row, g] == sc, (c, g, hex(S[row, g]))
+            assert P[row, 8 * g:8 * g + 8].tolist() == pay, (c, g, P[row].tolist())
+
+
+def test_nvfp4_scores_equal_bf16_scorer_on_dequantised_cache():
+    """e2m1 x E4M3 values are exact in bf16 (ROCm/ATOM #2745, Validation): the
+    FP4 scorer must pick the same blocks as the bf16 scorer fed the dequantised
+    keys, with the same scores."""
+    spec = workloads.small_spec("eq", 401, "nvfp4", "bf16", R=5, len_range=(1, 8000), topk=32)
+    b = workloads.make_batch(spec)
+    payload, scale = _gpu.device_planes(b)
+    out4 = _gpu.run(b, planes=(payload, scale))
+    # dequantise the stored planes with the oracle, as bf16 keys
+    deq = oracle.formats.nvfp4_dequantize(np_u8(payload.cpu()), np_u8(scale.cpu()))
+    kb = torch.from_numpy(deq.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(kb.to(torch.float64), torch.from_numpy(deq))      # exact
+    b16 = workloads.Batch(**{**b.__dict__})
+    b16.spec = workloads.Spec(**{**spec.__dict__, "k_dtype": "bf16"})
+    b16.payload = kb.view(torch.uint8).reshape(-1, 256)
+    b16.scale = None
+    out16 = _gpu.run(b16, planes=(b16.payload.cuda(), None))
+    assert np.array_equal(out4.ids, out16.ids)
+    np.testing.assert_allclose(out4.scores, out16.scores, rtol=1e-6, atol=1e-6)
+
+
+def test_pad_requests_and_empty_rows():
+    spec = workloads.small_spec("pad", 501, "bf16", "bf16", R=4, P=2, G=2,
+                                explicit_lens=[[0, 0], [5, 300], [200, 200], [1, 1]],
+                                pad_requests=(2, 3), topk=4)
+    b = workloads.make_batch(spec)
+    out = _gpu.run(b)
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_all_rows(b, out, ref)
+    for r in (0, 2, 3):
+        assert np.all(out.ids[r] == -1) and np.all(np.isneginf(out.scores[r]))
+
+
+def test_zero_requests():
+    spec = workloads.small_spec("z", 502, "bf16", "bf16", R=1, len_range=(10, 20))
+    b = workloads.make_batch(spec)
+    import sparse_attention_indexer_packed_gb300 as idx
+    q = b.q[:0].cuda()
+    out_ids = torch.zeros((0, 16, 16), dtype=torch.int32, device="cuda")
+    out_sc = torch.zeros((0, 16, 16), dtype=torch.float32, device="cuda")
+    ws = idx.alloc_workspace(0, 4, 4, b.max_pages)
+    idx.idx_score_topk(q, None, b.payload.cuda(), None, "bf16", b.page_table.cuda(),
+                       b.slot_ids[:0].cuda(), b.row_lens[:0].cuda(), 4, 4, 1, 2, 16,
+                       out_ids, out_sc, ws)
+    torch.cuda.synchronize()
+
+
+def test_topk_edge_values():
+    """topk = init + local (no free choice), topk = 256, all scores equal."""
+    spec = workloads.small_spec("e", 503, "bf16", "bf16", R=3, len_range=(1, 40000), topk=6)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    kw = oracle_kwargs(b)
+    for topk, init, local in [(3, 1, 2), (256, 1, 4), (1, 0, 0), (2, 2, 0)]:
+        out = _gpu.run(b, planes=planes, topk=topk, init_blocks=init, local_blocks=local)
+        ref = oracle.index.index_step(**dict(kw, topk=topk, init_blocks=init, local_blocks=local))
+        _check_all_rows(b, out, ref, init, local)
+    # all keys zero -> every block max is 0: ties resolve to the lowest ids
+    zp = torch.zeros_like(b.payload).cuda()
+    out = _gpu.run(b, planes=(zp, None), topk=8, init_blocks=1, local_blocks=1)
+    zkw = dict(kw, payload=np.zeros_like(kw["payload"]), topk=8, init_blocks=1, local_blocks=1)
+    ref = oracle.index.index_step(**zkw)
+    assert np.array_equal(out.ids, ref.ids)
+
+
+def test_bad_page_ids_are_flagged_not_read():
+    spec = workloads.small_spec("bp", 504, "fp8_e4m3", "fp8_e4m3", R=2, len_range=(3000, 4000))
+    b = workloads.make_batch(spec)
+    pt = b.page_table.clone()
+    pt[int(b.slot_ids[0]), 3] = b.num_pages + 5
+    pt[int(b.slot_ids[1]), 0] = -7
+    out = _gpu.run(b, page_table=pt)
+    assert out.flags & 1
+
+
+def test_rows_longer_than_the_page_table_are_clamped():
+    spec = workloads.small_spec("cl", 505, "bf16", "bf16", R=2, explicit_lens=[[100, 200, 300, 400]] * 2)
+    b = workloads.make_batch(spec)
+    b.row_lens[1, 3] = b.max_pages * 64 + 500
+    out = _gpu.run(b)
+    assert out.flags & 4
+    b.row_lens[1, 3] = b.max_pages * 64
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_all_rows(b, out, ref)
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype", [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3"),
+                                             ("nvfp4", "bf16")])
+def test_results_do_not_depend_on_the_grid(k_dtype, q_dtype):
+    """Few CTAs force many blocks (and request boundaries) through each CTA's
+    stage ring; the outputs must be bitwise the same as with one CTA per SM,
+    and match the oracle."""
+    import sparse_attention_indexer_packed_gb300 as idx
+    spec = workloads.small_spec("grid", 601, k_dtype, q_dtype, R=7, len_range=(1, 30000), topk=24,
+                                pad_requests=(2,))
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    base = _gpu.run(b, planes=planes)
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_all_rows(b, base, ref)
+    try:
+        for lim in (1, 3, 13):
+            idx.idx_set_grid_limit(lim)
+            o = _gpu.run(b, planes=planes)
+            assert o.flags == 0, (lim, hex(o.flags))
+            assert np.array_equal(o.ids, base.ids), lim
+            assert np.array_equal(o.scores.view(np.uint32), base.scores.view(np.uint32)), lim
+    finally:
+        idx.idx_set_grid_limit(0)
+
+
+def test_batch_invariance_of_a_request():
+    """A request's outputs are bitwise the same whatever the other requests in
+    the batch are (reduction order never depends on the batch)."""
+    spec = workloads.small_spec("bi", 602, "bf16", "bf16", R=6, len_range=(500, 20000), topk=16)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    a = _gpu.run(b, planes=planes)
+    b2 = workloads.make_batch(spec)
+    g = torch.Generator().manual_seed(5)
+    b2.q[1:] = torch.randn(b2.q[1:].shape, generator=g).to(torch.bfloat16)
+    b2.row_lens[2:] = torch.randint(1, 20000, b2.row_lens[2:].shape, generator=g, dtype=torch.int32)
+    o = _gpu.run(b2, planes=planes)
+    assert np.array_equal(a.ids[0], o.ids[0])
+    assert np.array_equal(a.scores[0].view(np.uint32), o.scores[0].view(np.uint32))

@@ -76,6 +76,7 @@ class Batch:
     page_table: torch.Tensor          # int32 [n_slots, max_pages]
     slot_ids: torch.Tensor            # int32 [R]
     row_lens: torch.Tensor            # int32 [R, P]
+    staging_offsets: Optional[list] = None  # first staged row of each request (-1: pad)
 
     @property
     def R(self) -> int:
@@ -181,6 +182,7 @@ def make_batch(spec: Spec) -> Batch:
     # ---- pool contents: every row random, so a misaddressed read shows -----
     rows = num_pages * PAGE
     staging = slot_mapping = None
+    staging_offsets = None
     if spec.k_dtype == "bf16":
         payload = _bf16_rows(gen, rows).view(torch.uint8).reshape(rows, 256)
         scale = None
@@ -194,9 +196,14 @@ def make_batch(spec: Spec) -> Batch:
         scale = torch.randint(0, 0x7F, (rows, 8), generator=gen, dtype=torch.uint8)
         # the step's keys arrive as bf16 token-major staging + a slot mapping
         maps = []
+        staging_offsets = []
+        pos = 0
         for r in range(R):
             if r in spec.pad_requests:
+                staging_offsets.append(-1)
                 continue
+            staging_offsets.append(pos)
+            pos += longest[r]
             t = torch.arange(longest[r], dtype=torch.int64)
             pg = page_table[slot_ids[r]].to(torch.int64)[t // PAGE]
             maps.append(pg * PAGE + t % PAGE)
@@ -218,7 +225,8 @@ def make_batch(spec: Spec) -> Batch:
 
     return Batch(spec=spec, q=q, q_scale=q_scale, num_pages=num_pages, payload=payload,
                  scale=scale, staging=staging, slot_mapping=slot_mapping,
-                 page_table=page_table, slot_ids=slot_ids_t, row_lens=row_lens)
+                 page_table=page_table, slot_ids=slot_ids_t, row_lens=row_lens,
+                 staging_offsets=staging_offsets)
 
 
 # ---------------------------------------------------------------------------
