@@ -196,6 +196,39 @@ IDX_API int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dty
  * The events are used once and then forgotten. */
 IDX_API int idx_set_kernel_events(void* score_begin, void* score_end, void* topk_end);
 
+/*
+ * idx_score_topk_noalloc — idx_score_topk for callers that cannot allocate device
+ * memory.  (The pages have no counterpart: it is an addition of this library.)
+ *
+ * Who needs it: a caller whose device memory is owned by someone else — a serving
+ * engine whose memory pool must account for every byte, a plugin loaded into a host
+ * framework with no allocator hook — or a caller that cannot afford the device-wide
+ * synchronisation cudaMalloc / cudaFree may cause in the middle of a decode step,
+ * has no way to hand idx_score_topk a workspace.  This variant keeps its block-score
+ * scratch in a fixed array of IDX_NOALLOC_SCRATCH_BYTES inside the library instead;
+ * every GPU that loads the library holds that array until the process exits.
+ *
+ * Same arguments and outputs as idx_score_topk without the workspace.  The call must
+ * need at most IDX_NOALLOC_SCRATCH_BYTES of scratch, i.e.
+ *   256 + num_requests * packed_queries * gqa * ceil(max_pages / 2) * 4 bytes,
+ * otherwise it returns IDX_ERR_INVALID before any device work.  It calls no
+ * allocator.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last call's
+ * contents (the error-flag header is cleared by each call): calls that overlap on
+ * the GPU — on different streams, or from different host threads — race on it and
+ * must be serialised by the caller.  The device error flags of this variant are
+ * not exposed.
+ */
+#define IDX_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+IDX_API int idx_score_topk_noalloc(const void* q, const float* q_scale, int q_dtype,
+                                   const void* k_payload, const void* k_scale, int k_dtype,
+                                   int64_t num_pages, const int32_t* page_table, int n_slots,
+                                   int max_pages, const int32_t* slot_ids,
+                                   const int32_t* row_lens, int num_requests, int packed_queries,
+                                   int gqa, int init_blocks, int local_blocks, int topk,
+                                   int32_t* out_ids, float* out_scores, void* stream);
+
 /* idx_set_grid_limit — cap the number of CTAs the score kernel launches (process-
  * wide; 0 restores the default of one CTA per SM).  Results do not depend on it:
  * each block max is computed whole by one warp, so any split of the work gives the

@@ -56,6 +56,8 @@ _SIGNATURES = {
                             _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "idx_score_topk_perrow": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
                                    _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "idx_score_topk_noalloc": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
+                                    _I, _I, _I, _I, _P, _P, _P]),
     "idx_set_kernel_events": (_I, [_P, _P, _P]),
     "idx_set_grid_limit": (_I, [_I]),
     "idx_workspace_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -205,6 +207,23 @@ def idx_set_kernel_events(score_begin=None, score_end=None, topk_end=None) -> No
     """Arm torch.cuda.Event objects (enable_timing=True) for the next score call."""
     h = [None if e is None else e.cuda_event for e in (score_begin, score_end, topk_end)]
     _check(lib().idx_set_kernel_events(*h), "idx_set_kernel_events")
+
+
+def idx_score_topk_noalloc(q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids,
+                           row_lens, packed_queries, gqa, init_blocks, local_blocks, topk,
+                           out_ids, out_scores, stream=None) -> None:
+    """idx_score_topk with the library's fixed scratch array instead of a workspace,
+    for callers that cannot allocate device memory (see include/idx.h)."""
+    R = int(q.shape[0])
+    n_slots, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+    rc = lib().idx_score_topk_noalloc(
+        _dev(q, "q"), _dev(q_scale, "q_scale", required=False), _q_dtype(q),
+        _dev(k_payload, "k_payload"), _dev(k_scale, "k_scale", required=False), DTYPES[k_dtype],
+        int(k_payload.shape[0]) // PAGE, _dev(page_table, "page_table"), n_slots, max_pages,
+        _dev(slot_ids, "slot_ids"), _dev(row_lens, "row_lens"), R, packed_queries, gqa,
+        init_blocks, local_blocks, topk, _dev(out_ids, "out_ids"), _dev(out_scores, "out_scores"),
+        _stream_ptr(stream))
+    _check(rc, "idx_score_topk_noalloc")
 
 
 def idx_set_grid_limit(max_ctas: int) -> None:

@@ -202,6 +202,10 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
 
 }  // namespace
 
+namespace idx {
+int record_error(int status, const char* message) { return fail(status, "%s", message); }
+}  // namespace idx
+
 extern "C" {
 
 int idx_abi_version(void) { return IDX_ABI_VERSION; }

@@ -45,6 +45,9 @@ struct TopkArgs {
   int init_blocks, local_blocks, topk;
 };
 
+// Record an error message for idx_last_error() on this host thread; returns status.
+int record_error(int status, const char* message);
+
 // Process-wide cap on the score kernel's grid (0 = one CTA per SM).
 void set_grid_limit(int max_ctas);
 int grid_limit();
