@@ -232,6 +232,36 @@ def run_ours(args):
     score_ms = [e[0].elapsed_time(e[1]) for e in evs]
     topk_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
+    # ---- ablation: the same step with every draft row scored on its own -------
+    ablation = None
+    if not args.no_ablation:
+        n_ab = max(10, min(args.steps, 100))
+        for _ in range(3):
+            idx.idx_score_topk_perrow(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
+                                      s.packed_queries, s.gqa, s.init_blocks, s.local_blocks,
+                                      topk, out_ids, out_sc, wsp, stream)
+        abev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ab)]
+        for trio in abev:
+            for e in trio:
+                e.record(stream)
+        torch.cuda.synchronize(dev)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for k in range(n_ab):
+            idx.idx_set_kernel_events(*abev[k])
+            idx.idx_score_topk_perrow(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
+                                      s.packed_queries, s.gqa, s.init_blocks, s.local_blocks,
+                                      topk, out_ids, out_sc, wsp, stream)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ab_us = a0.elapsed_time(a1) * 1e3 / n_ab
+        ab_score = sum(e[0].elapsed_time(e[1]) for e in abev) / n_ab * 1e3
+        ablation = {"variant": "per-row (each draft row its own decode row, keys read P times)",
+                    "us_per_step": round(ab_us, 3), "score_us": round(ab_score, 3),
+                    "slowdown_vs_packed": round(ab_us / (total_ms / args.steps * 1e3), 3),
+                    "steps": n_ab}
+
     # ---- end to end through the public API with host buffers ------------------
     e2e = run_e2e(idx, batch, payload, scale, dev, stream, args)
 
@@ -281,6 +311,7 @@ def run_ours(args):
             "frac_of_8TBps": round(achieved / 8000.0, 4),
         },
         "e2e": e2e,
+        "ablation": ablation,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
@@ -439,6 +470,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-ablation", action="store_true", help="skip the per-row ablation timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

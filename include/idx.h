@@ -40,7 +40,7 @@ extern "C" {
 #define IDX_DIM 128
 #define IDX_MAX_PACKED_ROWS 16
 #define IDX_MAX_TOPK 256
-#define IDX_WORKSPACE_HEADER_BYTES 256
+#define IDX_WORKSPACE_HEADER_BYTES 1024
 
 typedef enum {
   IDX_BF16 = 0,      /* bfloat16 */
@@ -56,7 +56,8 @@ typedef enum {
   IDX_ERR_OOM = -4           /* device allocation failed */
 } idx_status;
 
-/* Device-side error flags, OR-ed into the first 4 bytes of the workspace. */
+/* Device-side error flags of a call, kept in the workspace header (read them with
+ * idx_workspace_errors). */
 #define IDX_DEVERR_BAD_PAGE 1u      /* a page id outside [0, num_pages): page not read */
 #define IDX_DEVERR_TIMEOUT 2u       /* a pipeline wait gave up (kernel ended early) */
 #define IDX_DEVERR_LEN_CLAMPED 4u   /* a row longer than max_pages * 64 was clamped */
@@ -115,9 +116,10 @@ IDX_API int idx_store_nvfp4(const void* src_bf16, const int64_t* slot_mapping, i
                     const idx_pool* pool, void* stream);
 
 /*
- * idx_score_topk_workspace_bytes — device scratch idx_score_topk needs: a 256-byte
- * header (device error flags) plus one fp32 block score per (request, packed row,
- * block): num_requests * packed_queries * gqa * ceil(max_pages / 2) floats.
+ * idx_score_topk_workspace_bytes — device scratch idx_score_topk needs: a header of
+ * IDX_WORKSPACE_HEADER_BYTES (device error flags) plus one fp32 block score per
+ * (request, packed row, block): num_requests * packed_queries * gqa *
+ * ceil(max_pages / 2) floats.
  */
 IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queries, int gqa,
                                       int max_pages);
@@ -153,8 +155,9 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  *   out_ids (device):    int32 [R][P*G][topk]
  *   out_scores (device): fp32 [R][P*G][topk]
  *   workspace (device):  >= idx_score_topk_workspace_bytes(R, P, G, max_pages) bytes,
- *                        256-byte aligned; overwritten; its first 4 bytes hold the
- *                        device error flags (IDX_DEVERR_*) of the call.
+ *                        256-byte aligned; overwritten by every call (no clearing is
+ *                        needed); its header holds the device error flags
+ *                        (IDX_DEVERR_*) of the last call.
  * Output row i of request r: its forced blocks in ascending id order, then the chosen
  * blocks by descending score (ties to the lower id), then (-1, -inf) pads.  Scores are
  * raw q.k block maxima (fp8: code dot products times q_scale times the key's scale).
@@ -162,7 +165,7 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  * Host-side checks return IDX_ERR_INVALID (P*G outside [1,16], topk out of range,
  * init+local > topk, NULL pointers, R < 0, n_slots or max_pages < 1, workspace too
  * small or misaligned, num_pages < 1).  With R == 0 only the workspace is required
- * (its header is cleared) and the per-request pointers may be NULL.
+ * (its header is reset) and the per-request pointers may be NULL.
  */
 IDX_API int idx_score_topk(const void* q, const float* q_scale, int q_dtype,
                    const void* k_payload, const void* k_scale, int k_dtype, int64_t num_pages,
@@ -210,12 +213,13 @@ IDX_API int idx_set_kernel_events(void* score_begin, void* score_end, void* topk
  *
  * Same arguments and outputs as idx_score_topk without the workspace.  The call must
  * need at most IDX_NOALLOC_SCRATCH_BYTES of scratch, i.e.
- *   256 + num_requests * packed_queries * gqa * ceil(max_pages / 2) * 4 bytes,
+ *   IDX_WORKSPACE_HEADER_BYTES + num_requests * packed_queries * gqa *
+ *   ceil(max_pages / 2) * 4 bytes,
  * otherwise it returns IDX_ERR_INVALID before any device work.  It calls no
  * allocator.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call before
  * any stream capture.  All calls share the one array and it keeps the last call's
- * contents (the error-flag header is cleared by each call): calls that overlap on
+ * contents (each call rewrites what it reads): calls that overlap on
  * the GPU — on different streams, or from different host threads — race on it and
  * must be serialised by the caller.  The device error flags of this variant are
  * not exposed.

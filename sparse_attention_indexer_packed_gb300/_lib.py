@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libidx.so")
 IDX_BF16, IDX_FP8_E4M3, IDX_NVFP4 = 0, 1, 2
 IDX_OK = 0
 PAGE, BLOCK, DIM = 64, 128, 128
-WORKSPACE_HEADER_BYTES = 256
+WORKSPACE_HEADER_BYTES = 1024
 DEVERR_BAD_PAGE, DEVERR_TIMEOUT, DEVERR_LEN_CLAMPED = 1, 2, 4
 
 DTYPES = {"bf16": IDX_BF16, "fp8_e4m3": IDX_FP8_E4M3, "nvfp4": IDX_NVFP4}

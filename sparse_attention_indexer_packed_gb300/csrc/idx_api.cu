@@ -14,6 +14,8 @@
 #include "../../include/idx.h"
 #include "idx_internal.cuh"
 
+static_assert(idx::kHeaderBytes == IDX_WORKSPACE_HEADER_BYTES, "header size mismatch");
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -143,9 +145,13 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
     return fail(IDX_ERR_INVALID, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(workspace, 0, IDX_WORKSPACE_HEADER_BYTES, st);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
-  if (R == 0) return IDX_OK;
+  cudaError_t e;
+  if (R == 0) {
+    // no kernel runs: record "no CTA, no flags" for idx_workspace_errors
+    e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace header");
+    return IDX_OK;
+  }
 
   CUtensorMap map;
   int rc = make_payload_map(k_dtype, k_payload, num_pages, &map);
@@ -160,7 +166,8 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
   sa.slot_ids = slot_ids;
   sa.row_lens = row_lens;
   sa.blockmax = reinterpret_cast<float*>(ws + IDX_WORKSPACE_HEADER_BYTES);
-  sa.err = reinterpret_cast<uint32_t*>(ws);
+  sa.err_bytes = ws + idx::kFlagBytesOff;
+  sa.err_count = reinterpret_cast<uint32_t*>(ws);
   sa.num_pages = num_pages;
   sa.n_slots = n_slots;
   sa.max_pages = max_pages;
@@ -183,7 +190,6 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
   ta.row_lens = row_lens;
   ta.out_ids = out_ids;
   ta.out_scores = out_scores;
-  ta.err = sa.err;
   ta.n_slots = n_slots;
   ta.max_pages = max_pages;
   ta.nb_cap = sa.nb_cap;
@@ -340,10 +346,17 @@ int idx_set_kernel_events(void* score_begin, void* score_end, void* topk_end) {
 int idx_workspace_errors(const void* workspace, void* stream, uint32_t* flags) {
   if (!workspace || !flags) return fail(IDX_ERR_INVALID, "a required pointer is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace flags");
+  uint8_t header[IDX_WORKSPACE_HEADER_BYTES];
+  cudaError_t e = cudaMemcpyAsync(header, workspace, sizeof(header), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace header");
   e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "synchronising the stream");
+  uint32_t n = 0;
+  memcpy(&n, header, sizeof(n));
+  if (n > (uint32_t)idx::kMaxScoreCtas) n = idx::kMaxScoreCtas;
+  uint32_t f = 0;
+  for (uint32_t c = 0; c < n; ++c) f |= header[idx::kFlagBytesOff + c];
+  *flags = f;
   return IDX_OK;
 }
 

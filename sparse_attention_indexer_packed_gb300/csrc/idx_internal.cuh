@@ -12,6 +12,11 @@ constexpr int kBlock = 128;   // tokens per scored block
 constexpr int kDim = 128;     // head dim
 constexpr int kTileRows = 16; // packed rows per dot tile
 constexpr int kMaxTopk = 256; // largest topk a call may ask for
+// Workspace header: word 0 = number of score CTAs of the last call, bytes
+// [kFlagBytesOff, kFlagBytesOff + that) = each CTA's device error flags.
+constexpr int kHeaderBytes = 1024;
+constexpr int kFlagBytesOff = 64;
+constexpr int kMaxScoreCtas = kHeaderBytes - kFlagBytesOff;
 
 // Key formats, matching idx_dtype.
 enum KeyFormat : int { kBf16 = 0, kFp8 = 1, kNvfp4 = 2 };
@@ -26,7 +31,8 @@ struct ScoreArgs {
   const int32_t* slot_ids;     // [R]
   const int32_t* row_lens;     // [R][P]
   float* blockmax;             // [R*P*G][nb_cap]
-  uint32_t* err;               // device error flags
+  uint8_t* err_bytes;          // one flag byte per CTA
+  uint32_t* err_count;         // CTAs that wrote a flag byte
   int64_t num_pages;
   int n_slots, max_pages, nb_cap;
   int R, P, G, M;
@@ -39,7 +45,6 @@ struct TopkArgs {
   const int32_t* row_lens;
   int32_t* out_ids;            // [R*M][topk]
   float* out_scores;
-  uint32_t* err;
   int n_slots, max_pages, nb_cap;
   int R, P, G, M;
   int init_blocks, local_blocks, topk;

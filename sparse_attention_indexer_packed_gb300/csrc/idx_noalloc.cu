@@ -57,7 +57,7 @@ extern "C" int idx_score_topk_noalloc(const void* q, const float* q_scale, int q
     return idx::record_error(IDX_ERR_INVALID,
                              "idx_score_topk_noalloc: this call needs more scratch than the "
                              "fixed array holds (num_requests * packed_queries * gqa * "
-                             "ceil(max_pages / 2) * 4 + 256 bytes must be <= "
+                             "ceil(max_pages / 2) * 4 + IDX_WORKSPACE_HEADER_BYTES must be <= "
                              "IDX_NOALLOC_SCRATCH_BYTES); use idx_score_topk with a workspace");
   void* scratch = nullptr;
   cudaError_t e = scratch_for_current_device(&scratch);

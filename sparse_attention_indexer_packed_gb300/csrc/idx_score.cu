@@ -11,18 +11,19 @@
 // How (sm_103a):
 //  * persistent grid, one CTA per SM; the flattened (group, block) work list is
 //    split into equal contiguous ranges, one per CTA;
-//  * warp 0 produces: it resolves pages through the slot table (a warp-wide
-//    gather for 32 blocks at a time) and issues TMA tensor loads of the 64-token
-//    pages into a ring of shared-memory stages (128-byte or 64-byte swizzle),
-//    plus 1-D bulk copies of the per-key scales, each stage completing on an
-//    mbarrier;
-//  * consumer warps each take whole 128-token blocks: ldmatrix from the swizzled
-//    stage, mma.sync with the query tile held in registers (bf16 m16n8k16, e4m3
-//    m16n8k32; NVFP4 keys are decoded to exact f16 in registers and use f16
-//    m16n8k16), masks by each row's length and reduces the block max with
-//    shuffles;
-//  * every wait is bounded: on timeout the CTA records IDX_DEVERR_TIMEOUT and
-//    winds down after its copies in flight have landed.
+//  * every warp of the CTA owns its own shared-memory stages: it resolves the
+//    pages of its next blocks through the slot table, issues TMA tensor loads
+//    of the 64-token pages (128-byte or 64-byte swizzle) plus 1-D bulk copies
+//    of the per-key scales into its stage, each stage completing on an
+//    mbarrier; after scoring a block it refills the same stage with its next
+//    block, so copies are issued by many warps at once and no stage is ever
+//    shared between warps;
+//  * scoring a block: ldmatrix from the swizzled stage, mma.sync with the query
+//    tile held in registers (bf16 m16n8k16, e4m3 m16n8k32; NVFP4 keys are
+//    decoded to exact f16 in registers and use f16 m16n8k16), a mask by each
+//    row's length and the block max by shuffles;
+//  * every wait is bounded: on timeout the warp records IDX_DEVERR_TIMEOUT and
+//    stops after its copies in flight have landed.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,7 +38,10 @@ namespace {
 
 constexpr uint32_t kErrBadPage = 1u;
 constexpr uint32_t kErrTimeout = 2u;
+constexpr uint32_t kErrLenClamped = 4u;
 
+// Warps and stages per key format.  Every warp is a consumer that also issues
+// the copies for its own stages (SPW stages per warp, S = NC * SPW in all).
 template <int KF>
 struct Cfg;
 
@@ -46,45 +50,47 @@ struct Cfg<kBf16> {
   static constexpr int kRowBytes = 256;
   static constexpr int kPagePayload = kPage * kRowBytes;  // 16 KB: two 8 KB swizzled boxes
   static constexpr int kScaleRow = 0;
-  static constexpr int kStages = 6;
-  static constexpr int kConsumers = 6;
+  static constexpr int kWarps = 6;
+  static constexpr int kStagesPerWarp = 1;
 };
 template <>
 struct Cfg<kFp8> {
   static constexpr int kRowBytes = 128;
   static constexpr int kPagePayload = kPage * kRowBytes;  // 8 KB: one swizzled box
   static constexpr int kScaleRow = 4;
-  static constexpr int kStages = 12;
-  static constexpr int kConsumers = 4;
+  static constexpr int kWarps = 12;
+  static constexpr int kStagesPerWarp = 1;
 };
 template <>
 struct Cfg<kNvfp4> {
   static constexpr int kRowBytes = 64;
   static constexpr int kPagePayload = kPage * kRowBytes;  // 4 KB: one 64B-swizzled box
   static constexpr int kScaleRow = 8;
-  static constexpr int kStages = 24;
-  static constexpr int kConsumers = 8;
+  static constexpr int kWarps = 20;
+  static constexpr int kStagesPerWarp = 1;
 };
 
-// Unit k of a CTA goes to stage k % S and consumer warp k % NC.  S is a multiple
-// of NC, so each stage is only ever read by one warp, which therefore waits on
-// its stage's phases strictly in order: a parity wait can never be satisfied by
-// the phase before the one it means.
+// Unit k of a CTA (one 128-token block) lives in stage k % S and is computed by
+// warp k % NC, which also issued its copies.  S is a multiple of NC, so each
+// stage belongs to one warp that fills and drains it strictly in order: a parity
+// wait can never be satisfied by the phase before the one it means, and no
+// "stage empty" barrier is needed.
 template <int KF>
 struct Layout {
-  static_assert(Cfg<KF>::kStages % Cfg<KF>::kConsumers == 0, "stages must split evenly");
+  static constexpr int NC = Cfg<KF>::kWarps;
+  static constexpr int S = NC * Cfg<KF>::kStagesPerWarp;
   static constexpr int kStagePayload = 2 * Cfg<KF>::kPagePayload;
   static constexpr int kPageScale = kPage * Cfg<KF>::kScaleRow;
   static constexpr int kStageScale = 2 * kPageScale;
-  static constexpr int S = Cfg<KF>::kStages;
   static constexpr int kPayloadOff = 0;
   static constexpr int kScaleOff = kPayloadOff + S * kStagePayload;
-  static constexpr int kBarOff = kScaleOff + S * kStageScale;        // full[S], empty[S]
-  static constexpr int kMetaOff = kBarOff + 2 * S * 8;               // int2 per stage
+  static constexpr int kBarOff = kScaleOff + S * kStageScale;        // full[S]
+  static constexpr int kMetaOff = kBarOff + S * 8;                   // int2 per stage
   static constexpr int kCtlOff = kMetaOff + S * 8;                   // control words
   static constexpr int kBytes = kCtlOff + 64;
   static constexpr int kSmemBytes = kBytes + 1024;                   // + alignment slack
-  static constexpr int kThreads = 32 * (1 + Cfg<KF>::kConsumers);
+  static constexpr int kThreads = 32 * NC;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct Group {
@@ -369,34 +375,102 @@ struct BlockScorer<kNvfp4> {
 };
 
 // ---------------------------------------------------------------------------
+// Walking a CTA's units: (group v, block b) of unit k, advanced across groups.
+// ---------------------------------------------------------------------------
+struct Walker {
+  int v, b, nbk, slot, extent;
+  __device__ void set(const ScoreArgs& a, int v_, int b_) {
+    const Group g = group_info(a, v_);
+    v = v_;
+    b = b_;
+    nbk = g.nbk;
+    slot = g.slot;
+    extent = g.extent;
+  }
+  // move n units forward; groups without blocks (pads, empty rows) are skipped
+  __device__ void advance(const ScoreArgs& a, int n, int V) {
+    b += n;
+    while (b >= nbk && v + 1 < V) {
+      b -= nbk;
+      set(a, v + 1, b);
+    }
+  }
+};
+
+// Physical pages of the unit a walker points at (-1: no second page, -2: bad
+// page id, not read).  Lanes 0 and 1 load one page-table entry each.
+__device__ __forceinline__ int load_page(const ScoreArgs& a, const Walker& w, int lane,
+                                         uint32_t* flags) {
+  int p = -1;
+  if (lane < 2) {
+    const bool want = lane == 0 || (w.b * kBlock + kPage) < w.extent;
+    if (want) {
+      p = __ldg(a.page_table + (size_t)w.slot * a.max_pages + 2 * w.b + lane);
+      if (p < 0 || p >= a.num_pages) {
+        atomicOr(flags, kErrBadPage);
+        p = -2;
+      }
+    }
+  }
+  return p;
+}
+
+// Issue the copies of one unit into stage s (lane 0 only).
+template <int KF>
+__device__ __forceinline__ void issue_unit(const ScoreArgs& a, const CUtensorMap* map,
+                                           uint32_t sbase, int s, int p0, int p1) {
+  using L = Layout<KF>;
+  using C = Cfg<KF>;
+  uint32_t tx = 0;
+  if (p0 >= 0) tx += C::kPagePayload + L::kPageScale;
+  if (p1 >= 0) tx += C::kPagePayload + L::kPageScale;
+  const uint32_t full = sbase + L::kBarOff + s * 8;
+  mbar_arrive_expect_tx(full, tx);
+  const uint32_t dst = sbase + L::kPayloadOff + s * L::kStagePayload;
+  const uint32_t sdst = sbase + L::kScaleOff + s * L::kStageScale;
+  const int pg[2] = {p0, p1};
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    if (pg[pp] < 0) continue;
+    const int y = pg[pp] * kPage;
+    if (KF == kBf16) {
+      // two 64-column boxes per page: d 0..63 and d 64..127
+      tma_load_2d(dst + pp * 8192, map, 0, y, full);
+      tma_load_2d(dst + 16384 + pp * 8192, map, 64, y, full);
+    } else {
+      tma_load_2d(dst + pp * C::kPagePayload, map, 0, y, full);
+      bulk_load(sdst + pp * L::kPageScale, a.k_scale + (size_t)pg[pp] * L::kPageScale,
+                L::kPageScale, full);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int KF>
 __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap payload_map) {
   using L = Layout<KF>;
-  using C = Cfg<KF>;
   constexpr int S = L::S;
-  constexpr int NC = C::kConsumers;
+  constexpr int NC = L::NC;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + L::kBarOff;
-  const uint32_t bar_empty = bar_full + S * 8;
   int2* meta = reinterpret_cast<int2*>(smem + L::kMetaOff);
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + L::kCtlOff);
-  // ctl[0] = units of this CTA, ctl[1] = first group, ctl[2] = first block, ctl[3] = abort
+  // ctl[0] = units of this CTA, ctl[1] = first group, ctl[2] = first block,
+  // ctl[4] = this CTA's device error flags (written out once, at the end)
+  unsigned int* cta_flags = reinterpret_cast<unsigned int*>(smem + L::kCtlOff) + 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full + s * 8, 1);
-      mbar_init(bar_empty + s * 8, 1);
-    }
+    for (int s = 0; s < S; ++s) mbar_init(bar_full + s * 8, 1);
     fence_barrier_init();
     prefetch_tensormap(&payload_map);
   }
@@ -405,9 +479,19 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   const int V = a.perrow ? a.R * a.P : a.R;
   if (warp == 0) {
     long long total = 0;
+    bool clamped = false;
     for (int v0 = 0; v0 < V; v0 += 32) {
       const int v = v0 + lane;
       int nbk = v < V ? group_info(a, v).nbk : 0;
+      if (v < V && blockIdx.x == 0) {
+        const int r = a.perrow ? v / a.P : v;
+        const int slot = __ldg(a.slot_ids + r);
+        if (slot >= 0 && slot < a.n_slots) {
+          const int j0 = a.perrow ? v - r * a.P : 0, j1 = a.perrow ? j0 + 1 : a.P;
+          for (int j = j0; j < j1; ++j)
+            clamped |= __ldg(a.row_lens + r * a.P + j) > a.max_pages * kPage;
+        }
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) nbk += __shfl_xor_sync(0xffffffffu, nbk, o);
       total += nbk;
@@ -436,131 +520,59 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       }
       prefix += __shfl_sync(0xffffffffu, incl, 31);
     }
+    clamped = __any_sync(0xffffffffu, clamped);
     if (lane == 0) {
       ctl[0] = (int)(u1 - u0);
       ctl[1] = v_start;
       ctl[2] = b_start;
-      ctl[3] = 0;
+      *cta_flags = clamped ? kErrLenClamped : 0u;
     }
   }
   __syncthreads();
   const int n_units = ctl[0];
+  // the top-k kernel may be scheduled now; it waits for this grid's completion
+  // (and memory) before reading the block maxima
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  if (warp == 0) {
-    // ======================= producer =======================================
-    int v = ctl[1], b = ctl[2];
-    Group gi = (n_units > 0) ? group_info(a, v) : Group{};
-    int issued = 0;
-    bool aborted = false;
-    for (int k0 = 0; k0 < n_units && !aborted; k0 += 32) {
-      // lane l describes unit k0 + l
-      int lv = v, lb = b + lane;
-      Group lg = gi;
-      while (lb >= lg.nbk && lv + 1 < V) {
-        lb -= lg.nbk;
-        ++lv;
-        lg = group_info(a, lv);
+  // ---- every warp: issue its own stages, then drain and refill them ---------
+  const int g = lane >> 2, t = lane & 3;
+  bool aborted = false;
+  int outstanding = -1;  // last unit issued into a stage and not yet drained
+  if (warp < n_units) {
+    Walker iw;  // next unit this warp issues: warp, warp + NC, warp + 2 NC, ...
+    iw.set(a, ctl[1], ctl[2]);
+    iw.advance(a, warp, V);
+    for (int j = 0; j < Cfg<KF>::kStagesPerWarp; ++j) {
+      const int kk = warp + j * NC;
+      if (kk >= n_units) break;
+      const int pg = load_page(a, iw, lane, cta_flags);
+      const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
+      if (lane == 0) {
+        meta[kk % S] = make_int2(iw.v, iw.b);
+        issue_unit<KF>(a, &payload_map, sbase, kk % S, p0, p1);
       }
-      int p0 = -1, p1 = -1;
-      if (k0 + lane < n_units) {
-        const int32_t* row = a.page_table + (size_t)lg.slot * a.max_pages;
-        p0 = __ldg(row + 2 * lb);
-        const bool two = (lb * kBlock + kPage) < lg.extent;
-        p1 = two ? __ldg(row + 2 * lb + 1) : -1;
-        const bool bad0 = p0 < 0 || p0 >= a.num_pages;
-        const bool bad1 = two && (p1 < 0 || p1 >= a.num_pages);
-        if (bad0 || bad1) atomicOr(a.err, kErrBadPage);
-        if (bad0) p0 = -2;
-        if (bad1) p1 = -2;
-      }
-      // next chunk starts one unit past lane 31's
-      {
-        const int v31 = __shfl_sync(0xffffffffu, lv, 31);
-        const int b31 = __shfl_sync(0xffffffffu, lb, 31);
-        v = v31;
-        b = b31 + 1;
-        gi = group_info(a, v);
-        while (b >= gi.nbk && v < V - 1) {
-          b -= gi.nbk;
-          ++v;
-          gi = group_info(a, v);
-        }
-      }
-      const int cnt = min(32, n_units - k0);
-      for (int u = 0; u < cnt; ++u) {
-        const int uv = __shfl_sync(0xffffffffu, lv, u);
-        const int ub = __shfl_sync(0xffffffffu, lb, u);
-        const int up0 = __shfl_sync(0xffffffffu, p0, u);
-        const int up1 = __shfl_sync(0xffffffffu, p1, u);
-        const int uslot = __shfl_sync(0xffffffffu, lg.slot, u);
-        (void)uslot;
-        if (lane == 0) {
-          const int k = k0 + u;
-          const int s = k % S;
-          if (k >= S) {
-            if (!mbar_wait_bounded(bar_empty + s * 8, ((k / S) - 1) & 1)) {
-              atomicOr(a.err, kErrTimeout);
-              ctl[3] = 1;
-              aborted = true;
-            }
-          }
-          if (!aborted && ctl[3]) aborted = true;
-          if (!aborted) {
-            meta[s] = make_int2(uv, ub);
-            uint32_t tx = 0;
-            if (up0 >= 0) tx += C::kPagePayload + L::kPageScale;
-            if (up1 >= 0) tx += C::kPagePayload + L::kPageScale;
-            const uint32_t full = bar_full + s * 8;
-            mbar_arrive_expect_tx(full, tx);
-            const uint32_t dst = sbase + L::kPayloadOff + s * L::kStagePayload;
-            const uint32_t sdst = sbase + L::kScaleOff + s * L::kStageScale;
-            const int pg[2] = {up0, up1};
-#pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-              if (pg[pp] < 0) continue;
-              const int y = pg[pp] * kPage;
-              if (KF == kBf16) {
-                // two 64-column boxes per page: d 0..63 and d 64..127
-                tma_load_2d(dst + pp * 8192, &payload_map, 0, y, full);
-                tma_load_2d(dst + 16384 + pp * 8192, &payload_map, 64, y, full);
-              } else {
-                tma_load_2d(dst + pp * C::kPagePayload, &payload_map, 0, y, full);
-                bulk_load(sdst + pp * L::kPageScale,
-                          a.k_scale + (size_t)pg[pp] * L::kPageScale, L::kPageScale, full);
-              }
-            }
-            issued = k + 1;
-          }
-        }
-        aborted = __shfl_sync(0xffffffffu, aborted ? 1 : 0, 0) != 0;
-        if (aborted) break;
-      }
+      outstanding = kk;
+      iw.advance(a, NC, V);
     }
-    // On abort, let the copies already issued land before the CTA exits.
-    if (lane == 0 && aborted) {
-      for (int k = max(0, issued - S); k < issued; ++k)
-        (void)mbar_wait_bounded(bar_full + (k % S) * 8, (k / S) & 1, 200000000ull);
-    }
-  } else {
-    // ======================= consumers ======================================
-    const int cw = warp - 1;
-    const int g = lane >> 2, t = lane & 3;
+
     int cur_v = -1;
     QTile<KF> qt;
     int L0 = 0, L1 = 0, row0 = -1, row1 = -1;
     float qs0 = 1.f, qs1 = 1.f;
-    for (int k = cw; k < n_units; k += NC) {
+    for (int k = warp; k < n_units; k += NC) {
       const int s = k % S;
-      if (ctl[3]) break;
       if (!mbar_wait_bounded(bar_full + s * 8, (k / S) & 1)) {
-        if (lane == 0) {
-          atomicOr(a.err, kErrTimeout);
-          ctl[3] = 1;
-        }
+        if (lane == 0) atomicOr(cta_flags, kErrTimeout);
+        aborted = true;
         break;
       }
+      __syncwarp();
       const int2 mt = meta[s];
       const int v = mt.x, b = mt.y;
+      // the unit that refills this stage: start its page-table loads now
+      const int kk = k + S;
+      const bool refill = kk < n_units;
+      const int pg = refill ? load_page(a, iw, lane, cta_flags) : -1;
       if (v != cur_v) {
         const Group gi = group_info(a, v);
         qt.load(a, gi.base_row, gi.nrows, lane);
@@ -580,8 +592,19 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       const int tbase = b * kBlock;
       float mx0 = -INFINITY, mx1 = -INFINITY;
       BlockScorer<KF>::run(qt, stage, scale_stage, scale_smem, lane, tbase, L0, L1, qs0, qs1, mx0, mx1);
+      // every lane's shared-memory reads of this stage are done; order them
+      // before the asynchronous copies that overwrite it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + s * 8);
+      const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
+      if (refill) {
+        if (lane == 0) {
+          meta[s] = make_int2(iw.v, iw.b);
+          issue_unit<KF>(a, &payload_map, sbase, s, p0, p1);
+        }
+        outstanding = kk;
+        iw.advance(a, NC, V);
+      }
 #pragma unroll
       for (int o = 1; o <= 2; o <<= 1) {
         mx0 = fmax_nan_free(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -596,6 +619,18 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
         if (row1 >= 0 && tbase < L1) a.blockmax[(size_t)row1 * a.nb_cap + b] = mx1;
       }
     }
+  }
+  // after a timeout, let this warp's copies still in flight land before exiting
+  if (aborted && lane == 0) {
+    for (int k = max(warp, outstanding - S + NC); k <= outstanding; k += NC)
+      if (k >= 0) (void)mbar_wait_bounded(bar_full + (k % S) * 8, (k / S) & 1, 200000000ull);
+  }
+  // publish this CTA's flags (one byte per CTA, overwritten by every call, so no
+  // clearing is needed between calls)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a.err_bytes[blockIdx.x] = (uint8_t)*cta_flags;
+    if (blockIdx.x == 0) *a.err_count = gridDim.x;
   }
 }
 
@@ -614,7 +649,8 @@ cudaError_t launch_kf(const ScoreArgs& a, const CUtensorMap& map, cudaStream_t s
                            L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int lim = g_grid_limit.load(std::memory_order_relaxed);
-  const int grid = (lim > 0 && lim < sms) ? lim : sms;
+  int grid = (lim > 0 && lim < sms) ? lim : sms;
+  if (grid > kMaxScoreCtas) grid = kMaxScoreCtas;
   score_kernel<KF><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, map);
   return cudaGetLastError();
 }

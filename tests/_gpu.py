@@ -46,7 +46,7 @@ def run(batch, perrow=False, planes=None, dev="cuda", topk=None, init_blocks=Non
     flags = idx.idx_workspace_errors(ws)
     torch.cuda.synchronize()
     nb_cap = (int(pt.shape[1]) + 1) // 2
-    bm = ws[256:256 + R * M * nb_cap * 4].view(torch.float32).reshape(R * M, nb_cap).cpu().numpy() \
+    bm = ws[1024:1024 + R * M * nb_cap * 4].view(torch.float32).reshape(R * M, nb_cap).cpu().numpy() \
         if R * M else np.zeros((0, nb_cap), np.float32)
     return GpuOut(ids=out_ids.cpu().numpy(), scores=out_sc.cpu().numpy(), flags=flags,
                   payload=payload, scale=scale, blockmax=bm)

@@ -40,9 +40,9 @@ def test_version_and_status_strings(L):
 
 
 def test_workspace_bytes(L):
-    assert idx.idx_score_topk_workspace_bytes(16, 4, 4, 2048) == 256 + 16 * 16 * 1024 * 4
-    assert idx.idx_score_topk_workspace_bytes(1, 1, 1, 3) == 256 + 2 * 4
-    assert idx.idx_score_topk_workspace_bytes(0, 4, 4, 10) == 256
+    assert idx.idx_score_topk_workspace_bytes(16, 4, 4, 2048) == 1024 + 16 * 16 * 1024 * 4
+    assert idx.idx_score_topk_workspace_bytes(1, 1, 1, 3) == 1024 + 2 * 4
+    assert idx.idx_score_topk_workspace_bytes(0, 4, 4, 10) == 1024
 
 
 FAKE = 0x10000  # a non-NULL, 256-aligned value; every case below fails validation first
