@@ -1,4 +1,4 @@
-// Block top-k select: one warp per packed output row.
+// Block top-k select: one CTA (eight warps) per packed output row.
 //
 // What it computes (sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring
 // for EAGLE verify rows", Modifications 1 and Accuracy Tests; sglang #45451,
@@ -8,14 +8,15 @@
 // the lower block id.  Output: forced blocks ascending, chosen blocks by
 // descending score, then (-1, -inf) pads.
 //
-// How: the non-forced candidates form one contiguous id range.  A warp copies
-// their scores into its own shared-memory slice as order-preserving 32-bit keys,
-// finds the k-th largest key with a most-significant-digit radix select (8-bit
-// digits starting below the bits every candidate shares, one warp-private
-// 256-bin histogram per digit), gathers the chosen ids with ballots, resolves
-// ties at the threshold to the lowest ids, and sorts the chosen (key desc, id
-// asc) with a bitonic network.  No block-wide barrier is involved; a CTA holds
-// up to eight rows.
+// How: the non-forced candidates form one contiguous id range.  Their block
+// maxima are read from L2 with many loads in flight per thread and kept in
+// shared memory as order-preserving 32-bit keys.  When there are many
+// candidates, most-significant-digit radix passes (8-bit digits starting below
+// the bits every candidate shares, one shared 256-bin histogram per digit)
+// narrow them to the keys at or above the threshold's bin, usually after one
+// pass.  Each remaining (key, id) entry is then placed by its rank among them,
+// ties going to the lower id; entries ranked c or later are dropped.  The score
+// written out is recovered from the key, so nothing is read back from memory.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -26,26 +27,44 @@ namespace idx {
 
 namespace {
 
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 16;  // independent loads in flight per thread
+// The exact step ranks at most kCap entries (kCap >= the largest topk).
+constexpr int kCap = 1024;
+static_assert(kCap >= kMaxTopk, "the exact step must hold a whole selection");
+
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f + 0.0f);  // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-struct WarpSmem {
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// composite sort key: larger score first, then lower id first
+__device__ __forceinline__ unsigned long long pack(uint32_t key, int id) {
+  return ((unsigned long long)key << 32) | (uint32_t)(0x7fffffff - id);
+}
+
+struct Shared {
   uint32_t hist[256];
-  unsigned long long sel[kMaxTopk];
+  unsigned long long sel[kCap];
+  uint32_t red_min[kWarps], red_max[kWarps];
+  int wsum[kWarps];
+  int count;
+  uint32_t digit, need, bin;
 };
 
-__global__ void topk_kernel(const TopkArgs a, int warps_per_cta) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * warps_per_cta + warp;
-  if (row >= a.R * a.M) return;
-  WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem)[warp];
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + (size_t)warps_per_cta * sizeof(WarpSmem)) +
-                   (size_t)warp * a.nb_cap;
+__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+  unsigned long long* sel = sh.sel;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  const int row = blockIdx.x;
   const int r = row / a.M;
   const int i = row - r * a.M;
   int32_t* out_ids = a.out_ids + (size_t)row * a.topk;
@@ -55,9 +74,6 @@ __global__ void topk_kernel(const TopkArgs a, int warps_per_cta) {
   const int slot = __ldg(a.slot_ids + r);
   int L = 0;
   if (slot >= 0 && slot < a.n_slots) L = min(__ldg(a.row_lens + r * a.P + i / a.G), a.max_pages * kPage);
-  // launched as a programmatic dependent of the score kernel: wait for its
-  // completion before touching the block maxima
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int nb = L > 0 ? (L + kBlock - 1) / kBlock : 0;
   const int fi = min(a.init_blocks, nb);       // forced init: [0, fi)
   const int ls = max(fi, nb - a.local_blocks);  // forced local: [ls, nb)
@@ -65,32 +81,33 @@ __global__ void topk_kernel(const TopkArgs a, int warps_per_cta) {
   const int ncand = ls - fi;                    // candidates: [fi, ls)
   const int c = min(a.topk, nb) - nf;           // candidates to choose
 
-  for (int t = lane; t < nf; t += 32) {
+  // pads need no block maxima: write them before waiting on the score kernel
+  for (int t = nf + max(c, 0) + tid; t < a.topk; t += kThreads) {
+    out_ids[t] = -1;
+    out_sc[t] = -INFINITY;
+  }
+  // launched as a programmatic dependent of the score kernel: wait for its
+  // completion before touching the block maxima
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int t = tid; t < nf; t += kThreads) {
     const int id = t < fi ? t : ls + (t - fi);
     out_ids[t] = id;
     out_sc[t] = bm[id];
   }
-  for (int t = nf + max(c, 0) + lane; t < a.topk; t += 32) {
-    out_ids[t] = -1;
-    out_sc[t] = -INFINITY;
-  }
   if (c <= 0) return;
 
   // ---- candidate keys ----------------------------------------------------
-  // 16 loads in flight per lane: the block maxima sit in L2, so the copy costs
-  // a couple of round trips rather than one per 32 candidates
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  constexpr int kBatch = 16;
-  for (int t0 = 0; t0 < ncand; t0 += 32 * kBatch) {
+  for (int t0 = 0; t0 < ncand; t0 += kThreads * kBatch) {
     float v[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int t = t0 + u * 32 + lane;
+      const int t = t0 + u * kThreads + tid;
       v[u] = t < ncand ? bm[fi + t] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int t = t0 + u * 32 + lane;
+      const int t = t0 + u * kThreads + tid;
       if (t < ncand) {
         const uint32_t k = order_key(v[u]);
         keys[t] = k;
@@ -104,135 +121,136 @@ __global__ void topk_kernel(const TopkArgs a, int warps_per_cta) {
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
-  __syncwarp();
+  if (lane == 0) {
+    sh.red_min[warp] = kmin;
+    sh.red_max[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = sh.red_min[0];
+  kmax = sh.red_max[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    kmin = min(kmin, sh.red_min[w]);
+    kmax = max(kmax, sh.red_max[w]);
+  }
 
-  uint32_t fixed_mask = 0, fixed_val = 0;
-  bool take_all_prefix = false;
-  uint32_t need = (uint32_t)c;
-  if (c == ncand) {
-    take_all_prefix = true;  // every candidate is chosen
-  } else if (kmin == kmax) {
-    fixed_mask = 0xffffffffu;  // all equal: ties resolved by id below
-    fixed_val = kmax;
-  } else {
+  // ---- narrow the candidates: radix passes on the threshold bin ----------
+  // After each pass the keys above the threshold bin are certainly chosen and
+  // the bin holds the rest; stop once "above + bin" is small enough to rank.
+  uint32_t fixed_mask = 0, fixed_val = 0, need = (uint32_t)c;
+  uint32_t ksize = (uint32_t)ncand;  // keys whose prefix is >= fixed_val
+  const uint32_t stop = max(2u * (uint32_t)c, (uint32_t)c + 64u);  // <= 512
+  if (ksize > stop && kmin != kmax) {
     int hi = 32 - __clz(kmin ^ kmax);  // bits [hi, 32) are common to all candidates
     fixed_mask = hi >= 32 ? 0u : (0xffffffffu << hi);
     fixed_val = kmax & fixed_mask;
-    while (hi > 0) {
+    while (hi > 0 && ksize > stop) {
       const int lo = max(hi - 8, 0);
       const uint32_t dmask = (1u << (hi - lo)) - 1u;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ws.hist[lane * 8 + e] = 0u;
-      __syncwarp();
-      for (int t = lane; t < ncand; t += 32) {
+      sh.hist[tid] = 0u;
+      __syncthreads();
+      for (int t = tid; t < ncand; t += kThreads) {
         const uint32_t k = keys[t];
-        if ((k & fixed_mask) == fixed_val) atomicAdd(&ws.hist[(k >> lo) & dmask], 1u);
+        if ((k & fixed_mask) == fixed_val) atomicAdd(&sh.hist[(k >> lo) & dmask], 1u);
       }
-      __syncwarp();
-      // bins from the top: lane l owns bins 255 - 8l - e, e = 0..7
-      uint32_t loc[8];
-      uint32_t sum = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        loc[e] = ws.hist[255 - 8 * lane - e];
-        sum += loc[e];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - sum;
-      const bool has = excl < need && need <= incl;
-      uint32_t digit = 0, rem = 0, all = 0;
-      if (has) {
-        uint32_t above = excl;
+      __syncthreads();
+      if (warp == 0) {
+        // bins from the top: lane l owns bins 255 - 8l - e, e = 0..7
+        uint32_t loc[8];
+        uint32_t sum = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          if (!digit && above + loc[e] >= need) {
-            digit = (uint32_t)(255 - 8 * lane - e) | 0x100u;  // bit 8 marks "found"
-            rem = need - above;
-            all = (loc[e] == need - above) ? 1u : 0u;
+          loc[e] = sh.hist[255 - 8 * lane - e];
+          sum += loc[e];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        if (excl < need && need <= incl) {
+          uint32_t above = excl;
+          for (int e = 0; e < 8; ++e) {
+            if (above + loc[e] >= need) {
+              sh.digit = (uint32_t)(255 - 8 * lane - e);
+              sh.need = need - above;
+              sh.bin = loc[e];
+              break;
+            }
+            above += loc[e];
           }
-          above += loc[e];
         }
       }
-      const int src = __ffs(__ballot_sync(0xffffffffu, has)) - 1;
-      digit = __shfl_sync(0xffffffffu, digit, src) & 0xffu;
-      need = __shfl_sync(0xffffffffu, rem, src);
-      all = __shfl_sync(0xffffffffu, all, src);
+      __syncthreads();
+      ksize = (uint32_t)c - sh.need + sh.bin;  // above the bin + in the bin
+      need = sh.need;
       fixed_mask |= dmask << lo;
-      fixed_val |= digit << lo;
-      __syncwarp();
-      if (all) {
-        take_all_prefix = true;
-        break;
-      }
+      fixed_val |= sh.digit << lo;
       hi = lo;
     }
   }
 
-  // ---- gather the chosen ids ---------------------------------------------
-  // above the threshold: (k & mask) > val; with take_all_prefix also == val
-  int count = 0;
-  for (int t0 = 0; t0 < ncand; t0 += 32) {
-    const int t = t0 + lane;
-    bool pick = false;
-    uint32_t k = 0;
-    if (t < ncand) {
-      k = keys[t];
-      const uint32_t km = k & fixed_mask;
-      pick = take_all_prefix ? (km >= fixed_val) : (km > fixed_val);
-    }
-    const unsigned m = __ballot_sync(0xffffffffu, pick);
-    const int pos = count + __popc(m & ((1u << lane) - 1u));
-    if (pick && pos < kMaxTopk)
-      ws.sel[pos] = ((unsigned long long)k << 32) | (uint32_t)(0x7fffffff - (fi + t));
-    count += __popc(m);
+  // ---- gather the final candidate set -------------------------------------
+  // small enough: every key with prefix >= fixed_val; otherwise (many keys equal
+  // to the exact threshold) the keys above it plus the `need` lowest ids equal
+  // to it.  Either way each entry is then placed by its rank.
+  const bool small = ksize <= (uint32_t)kCap;
+  int mine = 0;
+  for (int t = tid; t < ncand; t += kThreads) {
+    const uint32_t km = keys[t] & fixed_mask;
+    mine += (small ? (km >= fixed_val) : (km > fixed_val)) ? 1 : 0;
   }
-  if (!take_all_prefix) {
+  int incl = mine;  // inclusive prefix of the per-thread counts, in thread order
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.wsum[warp] = incl;
+  __syncthreads();
+  int base = incl - mine;
+  for (int w = 0; w < warp; ++w) base += sh.wsum[w];
+  if (tid == kThreads - 1) sh.count = base + mine;
+  for (int t = tid; t < ncand; t += kThreads) {
+    const uint32_t k = keys[t];
+    const uint32_t km = k & fixed_mask;
+    if (small ? (km >= fixed_val) : (km > fixed_val)) {
+      if (base < kCap) sel[base] = pack(k, fi + t);
+      ++base;
+    }
+  }
+  __syncthreads();
+  if (!small && warp == 0) {
     // ties at the threshold: the `need` lowest ids among keys equal to it
     uint32_t left = need;
+    int b = sh.count;
     for (int t0 = 0; t0 < ncand && left > 0; t0 += 32) {
       const int t = t0 + lane;
       const bool eq = t < ncand && (keys[t] & fixed_mask) == fixed_val;
       const unsigned m = __ballot_sync(0xffffffffu, eq);
-      const int rank = __popc(m & ((1u << lane) - 1u));
-      if (eq && (uint32_t)rank < left && count + rank < kMaxTopk)
-        ws.sel[count + rank] =
-            ((unsigned long long)keys[t] << 32) | (uint32_t)(0x7fffffff - (fi + t));
+      const int rk = __popc(m & ((1u << lane) - 1u));
+      if (eq && (uint32_t)rk < left && b + rk < kCap) sel[b + rk] = pack(keys[t], fi + t);
       const uint32_t took = min((uint32_t)__popc(m), left);
-      count += (int)took;
+      b += (int)took;
       left -= took;
     }
+    if (lane == 0) sh.count = b;
   }
+  __syncthreads();
 
-  // ---- sort (key desc, id asc) and write --------------------------------
-  int n2 = 1;
-  while (n2 < c) n2 <<= 1;
-  for (int t = c + lane; t < n2; t += 32) ws.sel[t] = 0ull;
-  __syncwarp();
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int t = lane; t < n2; t += 32) {
-        const int p = t ^ j;
-        if (p > t) {
-          const unsigned long long x = ws.sel[t], y = ws.sel[p];
-          const bool desc = (t & k) == 0;
-          if (desc ? (x < y) : (x > y)) {
-            ws.sel[t] = y;
-            ws.sel[p] = x;
-          }
-        }
-      }
-      __syncwarp();
+  // ---- place each entry by its rank (key desc, id asc); keep ranks < c ----
+  const int n = min(sh.count, kCap);
+  for (int e = tid; e < n; e += kThreads) {
+    const unsigned long long x = sel[e];
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) rank += sel[j] > x ? 1 : 0;
+    if (rank < c) {
+      out_ids[nf + rank] = 0x7fffffff - (int)(uint32_t)(x & 0xffffffffull);
+      out_sc[nf + rank] = key_value((uint32_t)(x >> 32));
     }
-  }
-  for (int t = lane; t < c; t += 32) {
-    const int id = 0x7fffffff - (int)(uint32_t)(ws.sel[t] & 0xffffffffull);
-    out_ids[nf + t] = id;
-    out_sc[nf + t] = bm[id];
   }
 }
 
@@ -241,18 +259,13 @@ __global__ void topk_kernel(const TopkArgs a, int warps_per_cta) {
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   const int rows = a.R * a.M;
   if (rows == 0) return cudaSuccess;
-  // as many rows per CTA (one warp each) as fit in ~96 KB of shared memory
-  const size_t per_warp = sizeof(WarpSmem) + (size_t)a.nb_cap * sizeof(uint32_t);
-  int wpc = (int)((96 * 1024) / per_warp);
-  wpc = wpc < 1 ? 1 : (wpc > 8 ? 8 : wpc);
-  const size_t smem = per_warp * wpc;
+  const size_t smem = sizeof(Shared) + (size_t)a.nb_cap * sizeof(uint32_t);
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = (rows + wpc - 1) / wpc;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((unsigned)(32 * wpc));
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -260,7 +273,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_kernel, a, wpc);
+  e = cudaLaunchKernelEx(&cfg, topk_kernel, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
