@@ -133,6 +133,23 @@ __device__ __forceinline__ int tile_row_len(const ScoreArgs& a, int v, int r, in
 
 __device__ __forceinline__ float fmax_nan_free(float a, float b) { return a > b ? a : b; }
 
+// Fold the four accumulator values of one 8-token slice into the running row
+// maxima: v0, v1 belong to row g (tokens t0, t0 + 1), v2, v3 to row g + 8.
+// kMask = false is for blocks that lie wholly inside every live row's length.
+template <bool kMask>
+__device__ __forceinline__ void take(float& mx0, float& mx1, float v0, float v1, float v2,
+                                     float v3, int t0, int L0, int L1) {
+  if (kMask) {
+    if (t0 < L0) mx0 = fmax_nan_free(mx0, v0);
+    if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, v1);
+    if (t0 < L1) mx1 = fmax_nan_free(mx1, v2);
+    if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, v3);
+  } else {
+    mx0 = fmax_nan_free(mx0, fmax_nan_free(v0, v1));
+    mx1 = fmax_nan_free(mx1, fmax_nan_free(v2, v3));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Query tiles in mma.sync A-fragment order.
 // ---------------------------------------------------------------------------
@@ -259,6 +276,7 @@ struct BlockScorer;
 
 template <>
 struct BlockScorer<kBf16> {
+  template <bool kMask>
   __device__ static void run(const QTile<kBf16>& qt, uint32_t stage, uint32_t /*scale_stage*/,
                              const float* /*scale_smem*/, int lane, int tbase, int L0, int L1,
                              float qs0, float qs1, float& mx0, float& mx1) {
@@ -281,10 +299,7 @@ struct BlockScorer<kBf16> {
         mma_bf16_16816(acc, qt.a[2 * c + 1], b2, b3);
       }
       const int t0 = tbase + nt * 8 + 2 * t;
-      if (t0 < L0) mx0 = fmax_nan_free(mx0, acc[0]);
-      if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, acc[1]);
-      if (t0 < L1) mx1 = fmax_nan_free(mx1, acc[2]);
-      if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, acc[3]);
+      take<kMask>(mx0, mx1, acc[0], acc[1], acc[2], acc[3], t0, L0, L1);
     }
     (void)qs0;
     (void)qs1;
@@ -293,6 +308,7 @@ struct BlockScorer<kBf16> {
 
 template <>
 struct BlockScorer<kFp8> {
+  template <bool kMask>
   __device__ static void run(const QTile<kFp8>& qt, uint32_t stage, uint32_t /*scale_stage*/,
                              const float* scale_smem, int lane, int tbase, int L0, int L1,
                              float qs0, float qs1, float& mx0, float& mx1) {
@@ -316,16 +332,15 @@ struct BlockScorer<kFp8> {
       const int jt = nt * 8 + 2 * t;  // token of acc[0] within the block
       const float2 ks = *reinterpret_cast<const float2*>(scale_smem + jt);
       const int t0 = tbase + jt;
-      if (t0 < L0) mx0 = fmax_nan_free(mx0, (acc[0] * qs0) * ks.x);
-      if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, (acc[1] * qs0) * ks.y);
-      if (t0 < L1) mx1 = fmax_nan_free(mx1, (acc[2] * qs1) * ks.x);
-      if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, (acc[3] * qs1) * ks.y);
+      take<kMask>(mx0, mx1, (acc[0] * qs0) * ks.x, (acc[1] * qs0) * ks.y, (acc[2] * qs1) * ks.x,
+                  (acc[3] * qs1) * ks.y, t0, L0, L1);
     }
   }
 };
 
 template <>
 struct BlockScorer<kNvfp4> {
+  template <bool kMask>
   __device__ static void run(const QTile<kNvfp4>& qt, uint32_t stage, uint32_t scale_stage,
                              const float* /*scale_smem*/, int lane, int tbase, int L0, int L1,
                              float /*qs0*/, float /*qs1*/, float& mx0, float& mx1) {
@@ -366,10 +381,7 @@ struct BlockScorer<kNvfp4> {
         mma_f16_16816(acc, qt.a[2 * mm + 1], k2, k3);
       }
       const int t0 = tbase + nt * 8 + 2 * t;
-      if (t0 < L0) mx0 = fmax_nan_free(mx0, acc[0]);
-      if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, acc[1]);
-      if (t0 < L1) mx1 = fmax_nan_free(mx1, acc[2]);
-      if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, acc[3]);
+      take<kMask>(mx0, mx1, acc[0], acc[1], acc[2], acc[3], t0, L0, L1);
     }
   }
 };
@@ -591,7 +603,15 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       const float* scale_smem = reinterpret_cast<const float*>(smem + L::kScaleOff + s * L::kStageScale);
       const int tbase = b * kBlock;
       float mx0 = -INFINITY, mx1 = -INFINITY;
-      BlockScorer<KF>::run(qt, stage, scale_stage, scale_smem, lane, tbase, L0, L1, qs0, qs1, mx0, mx1);
+      // most blocks lie inside every live row: score them without the mask
+      const bool whole = __all_sync(0xffffffffu, (row0 < 0 || tbase + kBlock <= L0) &&
+                                                     (row1 < 0 || tbase + kBlock <= L1));
+      if (whole)
+        BlockScorer<KF>::template run<false>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
+                                             L1, qs0, qs1, mx0, mx1);
+      else
+        BlockScorer<KF>::template run<true>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
+                                            L1, qs0, qs1, mx0, mx1);
       // every lane's shared-memory reads of this stage are done; order them
       // before the asynchronous copies that overwrite it
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
