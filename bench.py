@@ -143,6 +143,14 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_spec(spec, rank: int, world_size: int):
+    """The workload a rank scores: replicas draw their own inputs (seed offset by
+    rank) with the same shapes, so per-GPU work is fixed as N grows."""
+    if world_size <= 1:
+        return spec
+    return workloads.Spec(**{**spec.__dict__, "seed": spec.seed + 100 * rank})
+
+
 def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
@@ -171,9 +179,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     build_library()
 
-    spec = workloads.WORKLOADS[args.workload]
-    if ws_n > 1:
-        spec = workloads.Spec(**{**spec.__dict__, "seed": spec.seed + 100 * rank})
+    spec = replica_spec(workloads.WORKLOADS[args.workload], rank, ws_n)
     batch = workloads.make_batch(spec)
     s = batch.spec
     payload = batch.payload.to(dev)
