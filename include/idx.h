@@ -41,6 +41,7 @@ extern "C" {
 #define IDX_MAX_PACKED_ROWS 16
 #define IDX_MAX_TOPK 256
 #define IDX_WORKSPACE_HEADER_BYTES 1024
+#define IDX_MAX_REQUESTS 2048  /* per idx_score_topk call (draft rows per per-row call) */
 
 typedef enum {
   IDX_BF16 = 0,      /* bfloat16 */
@@ -157,13 +158,17 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  *   workspace (device):  >= idx_score_topk_workspace_bytes(R, P, G, max_pages) bytes,
  *                        256-byte aligned; overwritten by every call (no clearing is
  *                        needed); its header holds the device error flags
- *                        (IDX_DEVERR_*) of the last call.
+ *                        (IDX_DEVERR_*) of the last call and the state of the
+ *                        kernel's dynamic work counter, which every call leaves
+ *                        ready for the next one (a fresh workspace simply runs
+ *                        its first call with a static schedule).
  * Output row i of request r: its forced blocks in ascending id order, then the chosen
  * blocks by descending score (ties to the lower id), then (-1, -inf) pads.  Scores are
  * raw q.k block maxima (fp8: code dot products times q_scale times the key's scale).
  * Asynchronous on stream; allocates nothing; capturable in a CUDA graph.
  * Host-side checks return IDX_ERR_INVALID (P*G outside [1,16], topk out of range,
- * init+local > topk, NULL pointers, R < 0, n_slots or max_pages < 1, workspace too
+ * init+local > topk, NULL pointers, R < 0 or > IDX_MAX_REQUESTS, n_slots or
+ * max_pages < 1, workspace too
  * small or misaligned, num_pages < 1).  With R == 0 only the workspace is required
  * (its header is reset) and the per-request pointers may be NULL.
  */

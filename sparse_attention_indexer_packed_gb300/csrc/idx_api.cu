@@ -124,6 +124,10 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
                        (k_dtype == IDX_NVFP4 && q_dtype == IDX_BF16);
   if (!pair_ok)
     return fail(IDX_ERR_UNSUPPORTED, "unsupported (k_dtype, q_dtype) = (%d, %d)", k_dtype, q_dtype);
+  if ((perrow ? (long long)R * P : (long long)R) > idx::kMaxGroups)
+    return fail(IDX_ERR_INVALID, "at most %d %s per call (got %lld)", idx::kMaxGroups,
+                perrow ? "draft rows (num_requests * packed_queries)" : "requests",
+                perrow ? (long long)R * P : (long long)R);
   if (n_slots < 1 || max_pages < 1 || max_pages > 65536)
     return fail(IDX_ERR_INVALID, "need n_slots >= 1 and 1 <= max_pages <= 65536 (got %d, %d)",
                 n_slots, max_pages);
@@ -168,6 +172,8 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
   sa.blockmax = reinterpret_cast<float*>(ws + IDX_WORKSPACE_HEADER_BYTES);
   sa.err_bytes = ws + idx::kFlagBytesOff;
   sa.err_count = reinterpret_cast<uint32_t*>(ws);
+  sa.sched_counter = reinterpret_cast<uint32_t*>(ws + idx::kSchedOff);
+  sa.sched_tag = reinterpret_cast<const unsigned long long*>(ws + idx::kTagOff);
   sa.num_pages = num_pages;
   sa.n_slots = n_slots;
   sa.max_pages = max_pages;
@@ -190,6 +196,8 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
   ta.row_lens = row_lens;
   ta.out_ids = out_ids;
   ta.out_scores = out_scores;
+  ta.sched_counter = sa.sched_counter;
+  ta.sched_tag = reinterpret_cast<unsigned long long*>(ws + idx::kTagOff);
   ta.n_slots = n_slots;
   ta.max_pages = max_pages;
   ta.nb_cap = sa.nb_cap;

@@ -12,11 +12,20 @@ constexpr int kBlock = 128;   // tokens per scored block
 constexpr int kDim = 128;     // head dim
 constexpr int kTileRows = 16; // packed rows per dot tile
 constexpr int kMaxTopk = 256; // largest topk a call may ask for
-// Workspace header: word 0 = number of score CTAs of the last call, bytes
-// [kFlagBytesOff, kFlagBytesOff + that) = each CTA's device error flags.
+// Workspace header: word 0 = number of score CTAs of the last call; bytes
+// [kSchedOff, kSchedOff + 4) = the block counter of the dynamic schedule and
+// [kTagOff, kTagOff + 8) = kSchedTag once a call has left that counter at zero;
+// bytes [kFlagBytesOff, kFlagBytesOff + CTAs) = each CTA's device error flags.
 constexpr int kHeaderBytes = 1024;
+constexpr int kSchedOff = 8;
+constexpr int kTagOff = 16;
 constexpr int kFlagBytesOff = 64;
 constexpr int kMaxScoreCtas = kHeaderBytes - kFlagBytesOff;
+constexpr unsigned long long kSchedTag = 0x5CEDC0DE1DC0FFEEull;
+// Scoring groups a call may have (requests when packed, draft rows when per-row):
+// the score kernel keeps one prefix-sum entry and one slot per group in shared
+// memory.
+constexpr int kMaxGroups = 2048;
 
 // Key formats, matching idx_dtype.
 enum KeyFormat : int { kBf16 = 0, kFp8 = 1, kNvfp4 = 2 };
@@ -33,6 +42,8 @@ struct ScoreArgs {
   float* blockmax;             // [R*P*G][nb_cap]
   uint8_t* err_bytes;          // one flag byte per CTA
   uint32_t* err_count;         // CTAs that wrote a flag byte
+  uint32_t* sched_counter;     // dynamic-schedule block counter (zero at entry)
+  const unsigned long long* sched_tag;  // kSchedTag when the counter is valid
   int64_t num_pages;
   int n_slots, max_pages, nb_cap;
   int R, P, G, M;
@@ -45,6 +56,8 @@ struct TopkArgs {
   const int32_t* row_lens;
   int32_t* out_ids;            // [R*M][topk]
   float* out_scores;
+  uint32_t* sched_counter;     // reset to zero for the next call
+  unsigned long long* sched_tag;
   int n_slots, max_pages, nb_cap;
   int R, P, G, M;
   int init_blocks, local_blocks, topk;

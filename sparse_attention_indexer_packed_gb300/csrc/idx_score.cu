@@ -70,24 +70,23 @@ struct Cfg<kNvfp4> {
   static constexpr int kStagesPerWarp = 1;
 };
 
-// Unit k of a CTA (one 128-token block) lives in stage k % S and is computed by
-// warp k % NC, which also issued its copies.  S is a multiple of NC, so each
-// stage belongs to one warp that fills and drains it strictly in order: a parity
-// wait can never be satisfied by the phase before the one it means, and no
-// "stage empty" barrier is needed.
+// Each warp owns exactly one stage (one 128-token block: two pages) and fills
+// and drains it strictly in order, so a parity wait can never be satisfied by
+// the phase before the one it means and no "stage empty" barrier is needed.
 template <int KF>
 struct Layout {
+  static_assert(Cfg<KF>::kStagesPerWarp == 1, "one stage per warp");
   static constexpr int NC = Cfg<KF>::kWarps;
-  static constexpr int S = NC * Cfg<KF>::kStagesPerWarp;
+  static constexpr int S = NC;
   static constexpr int kStagePayload = 2 * Cfg<KF>::kPagePayload;
   static constexpr int kPageScale = kPage * Cfg<KF>::kScaleRow;
   static constexpr int kStageScale = 2 * kPageScale;
   static constexpr int kPayloadOff = 0;
   static constexpr int kScaleOff = kPayloadOff + S * kStagePayload;
   static constexpr int kBarOff = kScaleOff + S * kStageScale;        // full[S]
-  static constexpr int kMetaOff = kBarOff + S * 8;                   // int2 per stage
-  static constexpr int kCtlOff = kMetaOff + S * 8;                   // control words
-  static constexpr int kBytes = kCtlOff + 64;
+  static constexpr int kCtlOff = kBarOff + S * 8;                    // control words
+  static constexpr int kGroupOff = kCtlOff + 64;                     // group table
+  static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
   static constexpr int kSmemBytes = kBytes + 1024;                   // + alignment slack
   static constexpr int kThreads = 32 * NC;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -387,37 +386,33 @@ struct BlockScorer<kNvfp4> {
 };
 
 // ---------------------------------------------------------------------------
-// Walking a CTA's units: (group v, block b) of unit k, advanced across groups.
+// Work units: unit u (one 128-token block) of the call's flattened list is
+// block b of group v, found by binary search in the shared prefix table.
 // ---------------------------------------------------------------------------
-struct Walker {
-  int v, b, nbk, slot, extent;
-  __device__ void set(const ScoreArgs& a, int v_, int b_) {
-    const Group g = group_info(a, v_);
-    v = v_;
-    b = b_;
-    nbk = g.nbk;
-    slot = g.slot;
-    extent = g.extent;
+__device__ __forceinline__ void locate(const int* gpre, int V, int u, int& v, int& b) {
+  int lo = 0, hi = V - 1;  // largest v with gpre[v] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (gpre[mid] <= u) lo = mid;
+    else hi = mid - 1;
   }
-  // move n units forward; groups without blocks (pads, empty rows) are skipped
-  __device__ void advance(const ScoreArgs& a, int n, int V) {
-    b += n;
-    while (b >= nbk && v + 1 < V) {
-      b -= nbk;
-      set(a, v + 1, b);
-    }
-  }
-};
+  v = lo;
+  b = u - gpre[lo];
+}
 
-// Physical pages of the unit a walker points at (-1: no second page, -2: bad
-// page id, not read).  Lanes 0 and 1 load one page-table entry each.
-__device__ __forceinline__ int load_page(const ScoreArgs& a, const Walker& w, int lane,
-                                         uint32_t* flags) {
+// Page ids of block b of group v (-1: no second page, -2: bad page id, not
+// read).  Lanes 0 and 1 load one page-table entry each.  gslot[v] holds the
+// group's slot, with bit 31 set when its last block needs only one page.
+__device__ __forceinline__ int load_page(const ScoreArgs& a, const int* gpre, const int* gslot,
+                                         int v, int b, int lane, uint32_t* flags) {
   int p = -1;
   if (lane < 2) {
-    const bool want = lane == 0 || (w.b * kBlock + kPage) < w.extent;
+    const int word = gslot[v];
+    const int slot = word & 0x7fffffff;
+    const bool last = b == gpre[v + 1] - gpre[v] - 1;
+    const bool want = lane == 0 || !(last && word < 0);
     if (want) {
-      p = __ldg(a.page_table + (size_t)w.slot * a.max_pages + 2 * w.b + lane);
+      p = __ldg(a.page_table + (size_t)slot * a.max_pages + 2 * b + lane);
       if (p < 0 || p >= a.num_pages) {
         atomicOr(flags, kErrBadPage);
         p = -2;
@@ -464,187 +459,192 @@ template <int KF>
 __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap payload_map) {
   using L = Layout<KF>;
-  constexpr int S = L::S;
   constexpr int NC = L::NC;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + L::kBarOff;
-  int2* meta = reinterpret_cast<int2*>(smem + L::kMetaOff);
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + L::kCtlOff);
-  // ctl[0] = units of this CTA, ctl[1] = first group, ctl[2] = first block,
-  // ctl[4] = this CTA's device error flags (written out once, at the end)
+  // ctl[0] = units of the call, ctl[1] = first dynamically scheduled unit,
+  // ctl[2] = dynamic schedule on, ctl[4] = this CTA's device error flags
   unsigned int* cta_flags = reinterpret_cast<unsigned int*>(smem + L::kCtlOff) + 4;
+  int* gpre = reinterpret_cast<int*>(smem + L::kGroupOff);  // [V + 1] block prefix
+  int* gslot = gpre + kMaxGroups + 1;                      // [V] slot | one-page-last bit
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t bar = sbase + L::kBarOff + warp * 8;  // this warp's stage barrier
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(bar_full + s * 8, 1);
+  if (lane == 0) {
+    mbar_init(bar, 1);
     fence_barrier_init();
-    prefetch_tensormap(&payload_map);
   }
+  if (threadIdx.x == 0) prefetch_tensormap(&payload_map);
 
-  // ---- this CTA's contiguous share of the (group, block) work list ----------
+  // ---- group table: block prefix sums and slots of every group -------------
   const int V = a.perrow ? a.R * a.P : a.R;
   if (warp == 0) {
-    long long total = 0;
+    int run = 0;
     bool clamped = false;
     for (int v0 = 0; v0 < V; v0 += 32) {
       const int v = v0 + lane;
-      int nbk = v < V ? group_info(a, v).nbk : 0;
-      if (v < V && blockIdx.x == 0) {
-        const int r = a.perrow ? v / a.P : v;
-        const int slot = __ldg(a.slot_ids + r);
-        if (slot >= 0 && slot < a.n_slots) {
-          const int j0 = a.perrow ? v - r * a.P : 0, j1 = a.perrow ? j0 + 1 : a.P;
+      int nbk = 0, word = 0;
+      if (v < V) {
+        const Group gi = group_info(a, v);
+        nbk = gi.nbk;
+        const int rem = gi.extent - (nbk - 1) * kBlock;  // tokens in the last block
+        word = (nbk > 0 ? gi.slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
+        if (blockIdx.x == 0 && gi.slot >= 0 && gi.slot < a.n_slots) {
+          const int j0 = a.perrow ? v - gi.r * a.P : 0, j1 = a.perrow ? j0 + 1 : a.P;
           for (int j = j0; j < j1; ++j)
-            clamped |= __ldg(a.row_lens + r * a.P + j) > a.max_pages * kPage;
+            clamped |= __ldg(a.row_lens + gi.r * a.P + j) > a.max_pages * kPage;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) nbk += __shfl_xor_sync(0xffffffffu, nbk, o);
-      total += nbk;
-    }
-    const long long u0 = total * blockIdx.x / gridDim.x;
-    const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
-    long long prefix = 0;
-    int v_start = V, b_start = 0;
-    for (int v0 = 0; v0 < V && v_start == V; v0 += 32) {
-      const int v = v0 + lane;
-      const int nbk = v < V ? group_info(a, v).nbk : 0;
       int incl = nbk;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      const long long excl = prefix + incl - nbk;
-      const bool here = v < V && nbk > 0 && excl <= u0 && u0 < excl + nbk;
-      const unsigned hit = __ballot_sync(0xffffffffu, here);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        const long long ex = __shfl_sync(0xffffffffu, excl, src);
-        v_start = v0 + src;
-        b_start = (int)(u0 - ex);
+      if (v < V) {
+        gpre[v] = run + incl - nbk;
+        gslot[v] = word;
       }
-      prefix += __shfl_sync(0xffffffffu, incl, 31);
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
     clamped = __any_sync(0xffffffffu, clamped);
     if (lane == 0) {
-      ctl[0] = (int)(u1 - u0);
-      ctl[1] = v_start;
-      ctl[2] = b_start;
+      gpre[V] = run;
+      // long calls hand the last eighth of their blocks out at run time, which
+      // evens out the CTAs' finish times (measured: it pays from ~600 blocks per
+      // CTA; shorter calls lose more to query-tile reloads than they gain); only
+      // when a previous call left the counter at zero (its tag says so)
+      const bool dyn = *a.sched_tag == kSchedTag && run >= 600 * (int)gridDim.x;
+      ctl[0] = run;
+      ctl[1] = dyn ? run - run / 8 : run;
+      ctl[2] = dyn ? 1 : 0;
       *cta_flags = clamped ? kErrLenClamped : 0u;
     }
   }
   __syncthreads();
-  const int n_units = ctl[0];
   // the top-k kernel may be scheduled now; it waits for this grid's completion
   // (and memory) before reading the block maxima
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int U = ctl[0], Us = ctl[1];
+  const bool dyn = ctl[2] != 0;
+  const int s1 = (int)((long long)Us * (blockIdx.x + 1) / gridDim.x);
+  int sk = (int)((long long)Us * blockIdx.x / gridDim.x) + warp;  // next static unit
 
-  // ---- every warp: issue its own stages, then drain and refill them ---------
+  // this warp's units: its share of the CTA's static range, then blocks taken
+  // one at a time from the dynamic pool (the take is issued one unit ahead)
+  int ahead = -1;
+  if (dyn && lane == 0) ahead = Us + (int)atomicAdd(a.sched_counter, 1u);
+  auto next_unit = [&]() -> int {
+    if (sk < s1) {
+      const int u = sk;
+      sk += NC;
+      return u;
+    }
+    if (!dyn) return -1;
+    const int u = __shfl_sync(0xffffffffu, ahead, 0);
+    if (u >= U) return -1;
+    if (lane == 0) ahead = Us + (int)atomicAdd(a.sched_counter, 1u);
+    return u;
+  };
+
+  const uint32_t stage = sbase + L::kPayloadOff + warp * L::kStagePayload;
+  const uint32_t scale_stage = sbase + L::kScaleOff + warp * L::kStageScale;
+  const float* scale_smem = reinterpret_cast<const float*>(smem + L::kScaleOff + warp * L::kStageScale);
   const int g = lane >> 2, t = lane & 3;
   bool aborted = false;
-  int outstanding = -1;  // last unit issued into a stage and not yet drained
-  if (warp < n_units) {
-    Walker iw;  // next unit this warp issues: warp, warp + NC, warp + 2 NC, ...
-    iw.set(a, ctl[1], ctl[2]);
-    iw.advance(a, warp, V);
-    for (int j = 0; j < Cfg<KF>::kStagesPerWarp; ++j) {
-      const int kk = warp + j * NC;
-      if (kk >= n_units) break;
-      const int pg = load_page(a, iw, lane, cta_flags);
-      const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
-      if (lane == 0) {
-        meta[kk % S] = make_int2(iw.v, iw.b);
-        issue_unit<KF>(a, &payload_map, sbase, kk % S, p0, p1);
-      }
-      outstanding = kk;
-      iw.advance(a, NC, V);
-    }
+  uint32_t issued = 0;  // copies this warp has put into its stage
 
-    int cur_v = -1;
-    QTile<KF> qt;
-    int L0 = 0, L1 = 0, row0 = -1, row1 = -1;
-    float qs0 = 1.f, qs1 = 1.f;
-    for (int k = warp; k < n_units; k += NC) {
-      const int s = k % S;
-      if (!mbar_wait_bounded(bar_full + s * 8, (k / S) & 1)) {
-        if (lane == 0) atomicOr(cta_flags, kErrTimeout);
-        aborted = true;
-        break;
+  int cur = next_unit(), v_cur = 0, b_cur = 0;
+  if (cur >= 0) {
+    locate(gpre, V, cur, v_cur, b_cur);
+    const int pg = load_page(a, gpre, gslot, v_cur, b_cur, lane, cta_flags);
+    const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
+    if (lane == 0) issue_unit<KF>(a, &payload_map, sbase, warp, p0, p1);
+    ++issued;
+  }
+  int nxt = cur >= 0 ? next_unit() : -1, v_n = 0, b_n = 0, pg_n = -1;
+  if (nxt >= 0) {
+    locate(gpre, V, nxt, v_n, b_n);
+    pg_n = load_page(a, gpre, gslot, v_n, b_n, lane, cta_flags);
+  }
+
+  int cur_v = -1;
+  QTile<KF> qt;
+  int L0 = 0, L1 = 0, row0 = -1, row1 = -1;
+  float qs0 = 1.f, qs1 = 1.f;
+  while (cur >= 0) {
+    // a new group's query tile is loaded while the block's keys are in flight
+    if (v_cur != cur_v) {
+      const Group gi = group_info(a, v_cur);
+      qt.load(a, gi.base_row, gi.nrows, lane);
+      L0 = g < gi.nrows ? tile_row_len(a, v_cur, gi.r, g) : 0;
+      L1 = g + 8 < gi.nrows ? tile_row_len(a, v_cur, gi.r, g + 8) : 0;
+      row0 = g < gi.nrows ? gi.base_row + g : -1;
+      row1 = g + 8 < gi.nrows ? gi.base_row + g + 8 : -1;
+      if (KF == kFp8) {
+        qs0 = row0 >= 0 ? __ldg(a.q_scale + row0) : 0.f;
+        qs1 = row1 >= 0 ? __ldg(a.q_scale + row1) : 0.f;
       }
-      __syncwarp();
-      const int2 mt = meta[s];
-      const int v = mt.x, b = mt.y;
-      // the unit that refills this stage: start its page-table loads now
-      const int kk = k + S;
-      const bool refill = kk < n_units;
-      const int pg = refill ? load_page(a, iw, lane, cta_flags) : -1;
-      if (v != cur_v) {
-        const Group gi = group_info(a, v);
-        qt.load(a, gi.base_row, gi.nrows, lane);
-        L0 = g < gi.nrows ? tile_row_len(a, v, gi.r, g) : 0;
-        L1 = g + 8 < gi.nrows ? tile_row_len(a, v, gi.r, g + 8) : 0;
-        row0 = g < gi.nrows ? gi.base_row + g : -1;
-        row1 = g + 8 < gi.nrows ? gi.base_row + g + 8 : -1;
-        if (KF == kFp8) {
-          qs0 = row0 >= 0 ? __ldg(a.q_scale + row0) : 0.f;
-          qs1 = row1 >= 0 ? __ldg(a.q_scale + row1) : 0.f;
-        }
-        cur_v = v;
-      }
-      const uint32_t stage = sbase + L::kPayloadOff + s * L::kStagePayload;
-      const uint32_t scale_stage = sbase + L::kScaleOff + s * L::kStageScale;
-      const float* scale_smem = reinterpret_cast<const float*>(smem + L::kScaleOff + s * L::kStageScale);
-      const int tbase = b * kBlock;
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      // most blocks lie inside every live row: score them without the mask
-      const bool whole = __all_sync(0xffffffffu, (row0 < 0 || tbase + kBlock <= L0) &&
-                                                     (row1 < 0 || tbase + kBlock <= L1));
-      if (whole)
-        BlockScorer<KF>::template run<false>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
-                                             L1, qs0, qs1, mx0, mx1);
-      else
-        BlockScorer<KF>::template run<true>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
-                                            L1, qs0, qs1, mx0, mx1);
-      // every lane's shared-memory reads of this stage are done; order them
-      // before the asynchronous copies that overwrite it
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
-      if (refill) {
-        if (lane == 0) {
-          meta[s] = make_int2(iw.v, iw.b);
-          issue_unit<KF>(a, &payload_map, sbase, s, p0, p1);
-        }
-        outstanding = kk;
-        iw.advance(a, NC, V);
-      }
+      cur_v = v_cur;
+    }
+    if (!mbar_wait_bounded(bar, (issued - 1) & 1)) {
+      if (lane == 0) atomicOr(cta_flags, kErrTimeout);
+      aborted = true;
+      break;
+    }
+    __syncwarp();
+    const int tbase = b_cur * kBlock;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+    // most blocks lie inside every live row: score them without the mask
+    const bool whole = __all_sync(0xffffffffu, (row0 < 0 || tbase + kBlock <= L0) &&
+                                                   (row1 < 0 || tbase + kBlock <= L1));
+    if (whole)
+      BlockScorer<KF>::template run<false>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
+                                           L1, qs0, qs1, mx0, mx1);
+    else
+      BlockScorer<KF>::template run<true>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
+                                          L1, qs0, qs1, mx0, mx1);
+    // every lane's shared-memory reads of this stage are done; order them
+    // before the asynchronous copies that overwrite it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    const int p0 = __shfl_sync(0xffffffffu, pg_n, 0), p1 = __shfl_sync(0xffffffffu, pg_n, 1);
+    if (nxt >= 0) {
+      if (lane == 0) issue_unit<KF>(a, &payload_map, sbase, warp, p0, p1);
+      ++issued;
+    }
 #pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        mx0 = fmax_nan_free(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmax_nan_free(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      if (KF == kNvfp4) {
-        mx0 *= qt.post_scale();
-        mx1 *= qt.post_scale();
-      }
-      if (t == 0) {
-        if (row0 >= 0 && tbase < L0) a.blockmax[(size_t)row0 * a.nb_cap + b] = mx0;
-        if (row1 >= 0 && tbase < L1) a.blockmax[(size_t)row1 * a.nb_cap + b] = mx1;
-      }
+    for (int o = 1; o <= 2; o <<= 1) {
+      mx0 = fmax_nan_free(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmax_nan_free(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (KF == kNvfp4) {
+      mx0 *= qt.post_scale();
+      mx1 *= qt.post_scale();
+    }
+    if (t == 0) {
+      if (row0 >= 0 && tbase < L0) a.blockmax[(size_t)row0 * a.nb_cap + b_cur] = mx0;
+      if (row1 >= 0 && tbase < L1) a.blockmax[(size_t)row1 * a.nb_cap + b_cur] = mx1;
+    }
+    cur = nxt;
+    v_cur = v_n;
+    b_cur = b_n;
+    if (cur < 0) break;
+    nxt = next_unit();
+    pg_n = -1;
+    if (nxt >= 0) {
+      locate(gpre, V, nxt, v_n, b_n);
+      pg_n = load_page(a, gpre, gslot, v_n, b_n, lane, cta_flags);
     }
   }
-  // after a timeout, let this warp's copies still in flight land before exiting
-  if (aborted && lane == 0) {
-    for (int k = max(warp, outstanding - S + NC); k <= outstanding; k += NC)
-      if (k >= 0) (void)mbar_wait_bounded(bar_full + (k % S) * 8, (k / S) & 1, 200000000ull);
-  }
+  // after a timeout, let this warp's copy still in flight land before exiting
+  if (aborted && lane == 0) (void)mbar_wait_bounded(bar, (issued - 1) & 1, 200000000ull);
   // publish this CTA's flags (one byte per CTA, overwritten by every call, so no
   // clearing is needed between calls)
   __syncthreads();

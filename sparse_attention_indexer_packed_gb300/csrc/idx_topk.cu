@@ -89,6 +89,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   // launched as a programmatic dependent of the score kernel: wait for its
   // completion before touching the block maxima
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the score kernel is done: leave its block counter at zero for the next call
+  if (row == 0 && tid == 0) {
+    *reinterpret_cast<volatile uint32_t*>(a.sched_counter) = 0u;
+    *reinterpret_cast<volatile unsigned long long*>(a.sched_tag) = kSchedTag;
+  }
   for (int t = tid; t < nf; t += kThreads) {
     const int id = t < fi ? t : ls + (t - fi);
     out_ids[t] = id;
