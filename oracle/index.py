@@ -81,6 +81,23 @@ def row_block_max(q: np.ndarray, keys: np.ndarray, length: int) -> np.ndarray:
                     dtype=np.float64)
 
 
+def row_block_lse(q: np.ndarray, keys: np.ndarray, length: int) -> np.ndarray:
+    """The log-sum-exp block score (sglang #45451, Accuracy Tests: selected-block
+    scores "max; lse"): lse[b] = ln sum over tokens t in
+    [128 b, min(128 b + 128, length)) of exp(q . k_t), natural log, raw scores."""
+    nb = num_blocks(length)
+    s = keys[:length] @ q
+    out = []
+    for b in range(nb):
+        blk = s[b * BLOCK:min((b + 1) * BLOCK, length)]
+        m = blk.max()
+        out.append(m + np.log(np.exp(blk - m).sum()))
+    return np.array(out, dtype=np.float64)
+
+
+BLOCK_SCORES = {"max": row_block_max, "lse": row_block_lse}
+
+
 def forced_blocks(nb: int, init_blocks: int, local_blocks: int) -> list:
     """The blocks a row always keeps: its first init_blocks and last
     local_blocks, from the row's own block count (sglang #42614, Modifications 1)."""
@@ -133,9 +150,10 @@ class StepResult:
 
 def index_step(*, q, q_dtype, q_scale, payload, scale, k_dtype, page_table, slot_ids,
                row_lens, packed_queries, gqa, init_blocks, local_blocks, topk,
-               requests=None) -> StepResult:
+               requests=None, block_score="max") -> StepResult:
     """The whole step for every request (or only ``requests``; other requests'
-    rows are left as pads in the result).
+    rows are left as pads in the result).  block_score: "max" (the block's
+    largest score) or "lse" (its log-sum-exp); ``blockmax`` holds whichever.
 
     q: [R, P, G, 128] bf16 bits (uint16) or e4m3 codes (uint8); q_scale: [R, P*G]
     fp32 or None; payload/scale: pool planes (uint8 rows); page_table int
@@ -167,7 +185,7 @@ def index_step(*, q, q_dtype, q_scale, payload, scale, k_dtype, page_table, slot
                 continue
             qs = None if q_scale is None else q_scale[r, i]
             qv = dequant_query(q_dtype, q[r, j, h], qs)
-            bm = row_block_max(qv, keys, L)
+            bm = BLOCK_SCORES[block_score](qv, keys, L)
             blockmax[(r, i)] = bm
             ids[r, i], scores[r, i] = select_row(bm, init_blocks, local_blocks, topk)
     return StepResult(ids=ids, scores=scores, blockmax=blockmax)

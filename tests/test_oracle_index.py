@@ -308,3 +308,64 @@ def test_nvfp4_dequant_of_a_hand_worked_group():
     scale[0, 1] = 0x30   # 0.5
     v = formats.nvfp4_dequantize(payload, scale)
     assert v[0, 16:20].tolist() == [3, -3, 0, 0.5]
+
+
+# ----------------------------------------------------------------------------
+# log-sum-exp block score
+# ----------------------------------------------------------------------------
+def _bruteforce_blocklse(qv, keys, L):
+    out = []
+    for b in range((L + 127) // 128):
+        ss = [math.fsum(float(qv[d]) * float(keys[t, d]) for d in range(keys.shape[1]))
+              for t in range(128 * b, min(128 * b + 128, L))]
+        m = max(ss)
+        out.append(m + math.log(math.fsum(math.exp(x - m) for x in ss)))
+    return out
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype", [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3")])
+def test_blocklse_bruteforce(k_dtype, q_dtype):
+    spec = workloads.small_spec("lse", 22, k_dtype, q_dtype, R=2, P=2, G=2,
+                                explicit_lens=[[130, 300], [1, 257]])
+    b = workloads.make_batch(spec)
+    kw = oracle_kwargs(b)
+    res = index.index_step(**kw, block_score="lse")
+    for r in range(b.R):
+        slot = int(b.slot_ids[r])
+        keys = index.dequant_keys(k_dtype, kw["payload"], kw["scale"],
+                                  index.key_rows(kw["page_table"], slot, int(b.row_lens[r].max())))
+        for i in range(b.M):
+            j, h = i // spec.gqa, i % spec.gqa
+            L = int(b.row_lens[r, j])
+            qs = None if kw["q_scale"] is None else kw["q_scale"][r, i]
+            qv = index.dequant_query(q_dtype, kw["q"][r, j, h], qs)
+            np.testing.assert_allclose(res.blockmax[(r, i)], _bruteforce_blocklse(qv, keys, L),
+                                       rtol=1e-12, atol=1e-9)
+
+
+def test_blocklse_closed_forms_and_bounds():
+    """n equal scores c give c + ln n; one token gives its score; in general
+    max <= lse <= max + ln(n valid tokens)."""
+    L = 300
+    kv = np.zeros((5 * 64, 128), np.float32)
+    kv[:L, 0] = 2.0                       # every score equals 2 (q = e_0)
+    kv[:L, 1] = np.random.default_rng(1).standard_normal(L)
+    payload = torch.from_numpy(kv).to(torch.bfloat16).view(torch.uint8).numpy()
+    q = np.zeros((1, 2, 1, 128), np.float32)
+    q[0, 0, 0, 0] = 1.0
+    q[0, 1, 0, 1] = 1.0
+    qb = np_bits16(torch.from_numpy(q).to(torch.bfloat16))
+    common = dict(q=qb, q_dtype="bf16", q_scale=None, payload=payload, scale=None, k_dtype="bf16",
+                  page_table=np.array([[0, 1, 2, 3, 4]], np.int32), slot_ids=np.array([0]),
+                  row_lens=np.array([[L, 257]]), packed_queries=2, gqa=1, init_blocks=0,
+                  local_blocks=0, topk=3)
+    lse = index.index_step(**common, block_score="lse")
+    mx = index.index_step(**common, block_score="max")
+    np.testing.assert_allclose(lse.blockmax[(0, 0)], [2 + math.log(128), 2 + math.log(128),
+                                                      2 + math.log(44)], rtol=1e-12)
+    # row 1 (257 tokens): its last block holds one token, so lse = that score
+    assert lse.blockmax[(0, 1)][-1] == mx.blockmax[(0, 1)][-1]
+    counts = [128, 128, 1]
+    for b in range(3):
+        m, v = mx.blockmax[(0, 1)][b], lse.blockmax[(0, 1)][b]
+        assert m <= v <= m + math.log(counts[b]) + 1e-12
