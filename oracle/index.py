@@ -95,9 +95,6 @@ def row_block_lse(q: np.ndarray, keys: np.ndarray, length: int) -> np.ndarray:
     return np.array(out, dtype=np.float64)
 
 
-BLOCK_SCORES = {"max": row_block_max, "lse": row_block_lse}
-
-
 def forced_blocks(nb: int, init_blocks: int, local_blocks: int) -> list:
     """The blocks a row always keeps: its first init_blocks and last
     local_blocks, from the row's own block count (sglang #42614, Modifications 1)."""
@@ -185,7 +182,12 @@ def index_step(*, q, q_dtype, q_scale, payload, scale, k_dtype, page_table, slot
                 continue
             qs = None if q_scale is None else q_scale[r, i]
             qv = dequant_query(q_dtype, q[r, j, h], qs)
-            bm = BLOCK_SCORES[block_score](qv, keys, L)
+            if block_score == "max":
+                bm = row_block_max(qv, keys, L)
+            elif block_score == "lse":
+                bm = row_block_lse(qv, keys, L)
+            else:
+                raise ValueError(block_score)
             blockmax[(r, i)] = bm
             ids[r, i], scores[r, i] = select_row(bm, init_blocks, local_blocks, topk)
     return StepResult(ids=ids, scores=scores, blockmax=blockmax)
