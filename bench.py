@@ -166,6 +166,31 @@ def max_over_ranks(x: float, ws: int, dev) -> float:
     return float(t.item())
 
 
+def metric_name(args) -> str:
+    """The headline metric on the default workload with the block-max score;
+    any other workload or block score is named in the metric itself."""
+    if args.workload == DEFAULT_WORKLOAD and args.block_score == "max":
+        return METRIC
+    suffix = "" if args.block_score == "max" else f", {args.block_score} block score"
+    return f"index-step µs/layer ({args.workload}{suffix})"
+
+
+def workload_config(s, R, args, ws_n) -> dict:
+    """The workload's own keys in the JSON line's config (both arms)."""
+    return {
+        "workload": args.workload, "requests": R, "packed_queries": s.packed_queries,
+        "gqa": s.gqa, "k_dtype": s.k_dtype, "q_dtype": s.q_dtype,
+        "context": (f"U[{s.len_range[0]},{s.len_range[1]}]" if s.len_range else "explicit"),
+        "topk": s.topk, "init_blocks": s.init_blocks, "local_blocks": s.local_blocks,
+        "block_score": args.block_score,
+        "block": 128, "page": 64, "parallelism": f"replicas x{ws_n}",
+    }
+
+
+def score_fn(idx, args):
+    return idx.idx_score_topk_lse if args.block_score == "lse" else idx.idx_score_topk
+
+
 def run_ours(args):
     import sparse_attention_indexer_packed_gb300 as idx
     from sparse_attention_indexer_packed_gb300.build import build_library
@@ -198,12 +223,14 @@ def run_ours(args):
     wsp = idx.alloc_workspace(R, s.packed_queries, s.gqa, batch.max_pages, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    fn = score_fn(idx, args)
+
     def step(events=None):
         if events is not None:
             idx.idx_set_kernel_events(*events)
-        idx.idx_score_topk(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
-                           s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, topk,
-                           out_ids, out_sc, wsp, stream)
+        fn(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
+           s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, topk,
+           out_ids, out_sc, wsp, stream)
 
     for _ in range(args.warmup):
         step()
@@ -301,7 +328,7 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = ms_per_step * 1e3 / 1.0   # µs per step on each rank (replicas run concurrently)
     line = {
-        "metric": METRIC if args.workload == DEFAULT_WORKLOAD else f"index-step µs/layer ({args.workload})",
+        "metric": metric_name(args),
         "value": round(value, 3),
         "unit": "us",
         "n_gpus": ws_n,
@@ -315,11 +342,7 @@ def run_ours(args):
         "dtype": {"bf16": "bf16", "fp8_e4m3": "e4m3", "nvfp4": "e2m1xe4m3/bf16"}[s.k_dtype],
         "data": "synthetic",
         "config": {
-            "workload": args.workload, "requests": R, "packed_queries": s.packed_queries,
-            "gqa": s.gqa, "k_dtype": s.k_dtype, "q_dtype": s.q_dtype,
-            "context": (f"U[{s.len_range[0]},{s.len_range[1]}]" if s.len_range else "explicit"),
-            "topk": topk, "init_blocks": s.init_blocks, "local_blocks": s.local_blocks,
-            "block": 128, "page": 64, "parallelism": f"replicas x{ws_n}",
+            **workload_config(s, R, args, ws_n),
             "l2": f"inputs larger than L2 ({ab['keys'] / 1e6:.0f} MB of keys read per step), no flush",
             "aggregate_GBps": round(ws_n * ab["score"] / (ms_per_step * 1e-3) / 1e9, 1),
         },
@@ -370,6 +393,7 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
     wsp = idx.alloc_workspace(R, s.packed_queries, s.gqa, batch.max_pages, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in [hq, hpt, hsl, hln] + ([hqs] if hqs is not None else []))
     d2h = hid.numel() * 4 + hsc.numel() * 4
+    fn = score_fn(idx, args)
 
     def step():
         dq.copy_(hq, non_blocking=True)
@@ -378,8 +402,8 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
         dpt.copy_(hpt, non_blocking=True)
         dsl.copy_(hsl, non_blocking=True)
         dln.copy_(hln, non_blocking=True)
-        idx.idx_score_topk(dq, dqs, payload, scale, s.k_dtype, dpt, dsl, dln, s.packed_queries,
-                           s.gqa, s.init_blocks, s.local_blocks, topk, did, dsc, wsp, stream)
+        fn(dq, dqs, payload, scale, s.k_dtype, dpt, dsl, dln, s.packed_queries,
+           s.gqa, s.init_blocks, s.local_blocks, topk, did, dsc, wsp, stream)
         hid.copy_(did, non_blocking=True)
         hsc.copy_(dsc, non_blocking=True)
 
@@ -401,14 +425,14 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
                     "slot ids and row lengths are copied in, ids and scores copied out"}
 
 
-def _oracle_sample(batch, budget_s: float):
+def _oracle_sample(batch, budget_s: float, block_score: str = "max"):
     """Time the oracle on request 0 with its rows cut to n tokens; returns
     (seconds per token-row, n, cores)."""
     import oracle
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from _util import oracle_kwargs
     s = batch.spec
-    kw = oracle_kwargs(batch)
+    kw = dict(oracle_kwargs(batch), block_score=block_score)
     r0 = next(r for r in range(batch.R) if batch.group_lens()[r] > 0)
     n = 4096
     while True:
@@ -436,7 +460,7 @@ def _cores() -> int:
 
 
 def cpu_baseline(batch, args) -> dict:
-    per_tok, n, dt = _oracle_sample(batch, budget_s=20.0)
+    per_tok, n, dt = _oracle_sample(batch, budget_s=20.0, block_score=args.block_score)
     total_rows = int(sum(batch.row_lens[r].clamp_min(0).sum() for r in range(batch.R)
                          if batch.group_lens()[r] > 0)) * batch.spec.gqa
     us = per_tok * total_rows * 1e6
@@ -452,13 +476,13 @@ def run_reference(args):
     spec = workloads.WORKLOADS[args.workload]
     batch = workloads.make_batch(spec)
     budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
-    per_tok, n, dt = _oracle_sample(batch, budget_s=budget * 4)
+    per_tok, n, dt = _oracle_sample(batch, budget_s=budget * 4, block_score=args.block_score)
     total_rows = int(sum(batch.row_lens[r].clamp_min(0).sum() for r in range(batch.R)
                          if batch.group_lens()[r] > 0)) * spec.gqa
     import oracle
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from _util import oracle_kwargs
-    kw = oracle_kwargs(batch)
+    kw = dict(oracle_kwargs(batch), block_score=args.block_score)
     r0 = next(r for r in range(batch.R) if batch.group_lens()[r] > 0)
     lens = np.minimum(kw["row_lens"][r0:r0 + 1], n)
     kw1 = dict(kw, q=kw["q"][r0:r0 + 1], q_scale=None if kw["q_scale"] is None else kw["q_scale"][r0:r0 + 1],
@@ -476,11 +500,11 @@ def run_reference(args):
               f"scaled by token-rows to the whole step")
     line = {
         "impl": "reference",
-        "metric": METRIC if args.workload == DEFAULT_WORKLOAD else f"index-step µs/layer ({args.workload})",
+        "metric": metric_name(args),
         "value": round(us, 1), "unit": "us", "n_gpus": ws_n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "requests": batch.R},
+        "config": workload_config(spec, batch.R, args, ws_n),
         "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -495,6 +519,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--block-score", default="max", choices=["max", "lse"],
+                    help="block score the selection ranks by (max: the headline step)")
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-row ablation timing")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -182,6 +182,22 @@ IDX_API int idx_score_topk(const void* q, const float* q_scale, int q_dtype,
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * idx_score_topk_lse — idx_score_topk with the log-sum-exp block score in place of the
+ * block max (sglang #45451, Accuracy Tests: selected-block scores "max; lse"): a row's
+ * score for block b is ln sum exp(q.k_t) over the tokens t of the block inside the row's
+ * length (raw dot products, natural log).  Same arguments, outputs, selection rules and
+ * workspace; out_scores holds the chosen blocks' log-sum-exp.
+ */
+IDX_API int idx_score_topk_lse(const void* q, const float* q_scale, int q_dtype,
+                               const void* k_payload, const void* k_scale, int k_dtype,
+                               int64_t num_pages, const int32_t* page_table, int n_slots,
+                               int max_pages, const int32_t* slot_ids, const int32_t* row_lens,
+                               int num_requests, int packed_queries, int gqa,
+                               int init_blocks, int local_blocks, int topk,
+                               int32_t* out_ids, float* out_scores,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * idx_score_topk_perrow — the same step with every draft row scored as its own decode
  * row (the per-row kernel the packed one replaces: sglang #45451, Motivation; sglang
  * #42614, Motivation): the tile holds G live rows and each request's keys are read

@@ -54,6 +54,8 @@ _SIGNATURES = {
     "idx_score_topk_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "idx_score_topk": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I, _I,
                             _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "idx_score_topk_lse": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I, _I,
+                                _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "idx_score_topk_perrow": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
                                    _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "idx_score_topk_noalloc": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
@@ -191,6 +193,14 @@ def idx_score_topk(q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids
                    packed_queries, gqa, init_blocks, local_blocks, topk, out_ids, out_scores,
                    workspace, stream=None) -> None:
     _score("idx_score_topk", q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids,
+           row_lens, packed_queries, gqa, init_blocks, local_blocks, topk, out_ids, out_scores,
+           workspace, stream)
+
+
+def idx_score_topk_lse(q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids, row_lens,
+                       packed_queries, gqa, init_blocks, local_blocks, topk, out_ids, out_scores,
+                       workspace, stream=None) -> None:
+    _score("idx_score_topk_lse", q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids,
            row_lens, packed_queries, gqa, init_blocks, local_blocks, topk, out_ids, out_scores,
            workspace, stream)
 

@@ -104,7 +104,7 @@ int make_payload_map(int dtype, const void* payload, int64_t num_pages, CUtensor
   return IDX_OK;
 }
 
-int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtype,
+int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_scale, int q_dtype,
                     const void* k_payload, const void* k_scale, int k_dtype, int64_t num_pages,
                     const int32_t* page_table, int n_slots, int max_pages, const int32_t* slot_ids,
                     const int32_t* row_lens, int R, int P, int G, int init_blocks,
@@ -186,7 +186,7 @@ int score_topk_impl(bool perrow, const void* q, const float* q_scale, int q_dtyp
   cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
   g_ev[0] = g_ev[1] = g_ev[2] = nullptr;
   if (ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
-  e = idx::launch_score(k_dtype, sa, map, st);
+  e = idx::launch_score(k_dtype, block_score, sa, map, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
   if (ev[1] && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
 
@@ -319,10 +319,23 @@ int idx_score_topk(const void* q, const float* q_scale, int q_dtype, const void*
                    int num_requests, int packed_queries, int gqa, int init_blocks,
                    int local_blocks, int topk, int32_t* out_ids, float* out_scores,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  return score_topk_impl(false, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
+  return score_topk_impl(false, idx::kBlockMax, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
                          page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
                          packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
                          out_scores, workspace, workspace_bytes, stream);
+}
+
+int idx_score_topk_lse(const void* q, const float* q_scale, int q_dtype, const void* k_payload,
+                       const void* k_scale, int k_dtype, int64_t num_pages,
+                       const int32_t* page_table, int n_slots, int max_pages,
+                       const int32_t* slot_ids, const int32_t* row_lens, int num_requests,
+                       int packed_queries, int gqa, int init_blocks, int local_blocks, int topk,
+                       int32_t* out_ids, float* out_scores, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return score_topk_impl(false, idx::kBlockLse, q, q_scale, q_dtype, k_payload, k_scale, k_dtype,
+                         num_pages, page_table, n_slots, max_pages, slot_ids, row_lens,
+                         num_requests, packed_queries, gqa, init_blocks, local_blocks, topk,
+                         out_ids, out_scores, workspace, workspace_bytes, stream);
 }
 
 int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dtype, const void* k_payload,
@@ -332,7 +345,7 @@ int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dtype, cons
                           int packed_queries, int gqa, int init_blocks, int local_blocks,
                           int topk, int32_t* out_ids, float* out_scores, void* workspace,
                           size_t workspace_bytes, void* stream) {
-  return score_topk_impl(true, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
+  return score_topk_impl(true, idx::kBlockMax, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
                          page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
                          packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
                          out_scores, workspace, workspace_bytes, stream);

@@ -29,6 +29,8 @@ constexpr int kMaxGroups = 2048;
 
 // Key formats, matching idx_dtype.
 enum KeyFormat : int { kBf16 = 0, kFp8 = 1, kNvfp4 = 2 };
+// Block scores: the block's largest score, or the log-sum-exp of its scores.
+enum BlockScore : int { kBlockMax = 0, kBlockLse = 1 };
 
 // Arguments of one scoring pass.  A "group" is the set of tile rows that share
 // one read of the keys: a whole request when packed, one draft row when per-row.
@@ -71,8 +73,8 @@ void set_grid_limit(int max_ctas);
 int grid_limit();
 
 // Launchers (return cudaSuccess or the launch error).
-cudaError_t launch_score(int key_format, const ScoreArgs& args, const CUtensorMap& payload_map,
-                         cudaStream_t stream);
+cudaError_t launch_score(int key_format, int block_score, const ScoreArgs& args,
+                         const CUtensorMap& payload_map, cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& args, cudaStream_t stream);
 cudaError_t launch_store_nvfp4(const uint16_t* src, const int64_t* slot_mapping, int64_t num_tokens,
                                uint8_t* payload, uint8_t* scale, int64_t num_rows,

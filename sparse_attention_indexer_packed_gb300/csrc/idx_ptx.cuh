@@ -168,6 +168,13 @@ __device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
   return d;
 }
 
+// 2^x, the PTX approximate base-2 exponential (2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

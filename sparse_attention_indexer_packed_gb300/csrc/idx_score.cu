@@ -70,14 +70,18 @@ struct Cfg<kNvfp4> {
   static constexpr int kStagesPerWarp = 1;
 };
 
-// Each warp owns exactly one stage (one 128-token block: two pages) and fills
-// and drains it strictly in order, so a parity wait can never be satisfied by
-// the phase before the one it means and no "stage empty" barrier is needed.
+// Each warp owns D stages (one 128-token block each: two pages) and cycles
+// through them strictly in order: its k-th block goes to stage k % D and is
+// waited for with phase parity (k / D) & 1.  No other warp touches them, so a
+// parity wait can never be satisfied by the phase before the one it means and
+// no "stage empty" barrier is needed.  With D > 1 the warp's next blocks are in
+// flight while it scores the current one.
 template <int KF>
 struct Layout {
-  static_assert(Cfg<KF>::kStagesPerWarp == 1, "one stage per warp");
   static constexpr int NC = Cfg<KF>::kWarps;
-  static constexpr int S = NC;
+  static constexpr int D = Cfg<KF>::kStagesPerWarp;
+  static_assert(D == 1 || D == 2, "one or two stages per warp");
+  static constexpr int S = NC * D;
   static constexpr int kStagePayload = 2 * Cfg<KF>::kPagePayload;
   static constexpr int kPageScale = kPage * Cfg<KF>::kScaleRow;
   static constexpr int kStageScale = 2 * kPageScale;
@@ -132,22 +136,91 @@ __device__ __forceinline__ int tile_row_len(const ScoreArgs& a, int v, int r, in
 
 __device__ __forceinline__ float fmax_nan_free(float a, float b) { return a > b ? a : b; }
 
-// Fold the four accumulator values of one 8-token slice into the running row
-// maxima: v0, v1 belong to row g (tokens t0, t0 + 1), v2, v3 to row g + 8.
-// kMask = false is for blocks that lie wholly inside every live row's length.
-template <bool kMask>
-__device__ __forceinline__ void take(float& mx0, float& mx1, float v0, float v1, float v2,
-                                     float v3, int t0, int L0, int L1) {
-  if (kMask) {
-    if (t0 < L0) mx0 = fmax_nan_free(mx0, v0);
-    if (t0 + 1 < L0) mx0 = fmax_nan_free(mx0, v1);
-    if (t0 < L1) mx1 = fmax_nan_free(mx1, v2);
-    if (t0 + 1 < L1) mx1 = fmax_nan_free(mx1, v3);
-  } else {
-    mx0 = fmax_nan_free(mx0, fmax_nan_free(v0, v1));
-    mx1 = fmax_nan_free(mx1, fmax_nan_free(v2, v3));
+// Per-lane running block scores of the two tile rows a lane holds (row g and
+// g + 8).  add() folds the four accumulator values of one 8-token slice: v0, v1
+// belong to row g (tokens t0, t0 + 1), v2, v3 to row g + 8; kMask = false is
+// for blocks that lie wholly inside every live row's length.  reduce() merges
+// the four lanes of a row; out0/out1 give the block score of rows g / g + 8.
+//
+// Block max (sglang #45451, Modifications / Accuracy Tests: "max").
+struct MaxScore {
+  float m0 = -INFINITY, m1 = -INFINITY;
+  float post = 1.f;  // exact power-of-two rescale of the raw dot products
+  __device__ __forceinline__ explicit MaxScore(float post_scale) : post(post_scale) {}
+  template <bool kMask>
+  __device__ __forceinline__ void add(float v0, float v1, float v2, float v3, int t0, int L0,
+                                      int L1) {
+    if (kMask) {
+      if (t0 < L0) m0 = fmax_nan_free(m0, v0);
+      if (t0 + 1 < L0) m0 = fmax_nan_free(m0, v1);
+      if (t0 < L1) m1 = fmax_nan_free(m1, v2);
+      if (t0 + 1 < L1) m1 = fmax_nan_free(m1, v3);
+    } else {
+      m0 = fmax_nan_free(m0, fmax_nan_free(v0, v1));
+      m1 = fmax_nan_free(m1, fmax_nan_free(v2, v3));
+    }
   }
-}
+  __device__ __forceinline__ void reduce() {
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      m0 = fmax_nan_free(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmax_nan_free(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+  }
+  // a positive power of two commutes with the max: applied once, to the result
+  __device__ __forceinline__ float out0() const { return m0 * post; }
+  __device__ __forceinline__ float out1() const { return m1 * post; }
+};
+
+// Block log-sum-exp (sglang #45451, Accuracy Tests: "lse"): ln sum exp(s) over
+// the block's valid tokens.  Kept per row as the running maximum m of the raw
+// dot products and the sum of 2^((x - m) c), c = post * log2(e), so every term
+// costs one fused multiply-add and one ex2; each call folds a lane's two values
+// of a row in with one rescale and no branch (a masked value enters as -inf and
+// adds 2^-inf = 0).  lse = (m c + log2 sum) ln 2.
+struct LseScore {
+  float m0 = -INFINITY, s0 = 0.f, m1 = -INFINITY, s1 = 0.f;
+  float c;
+  __device__ __forceinline__ explicit LseScore(float post_scale)
+      : c(post_scale * 1.4426950408889634f) {}
+  __device__ __forceinline__ void push2(float& m, float& s, float x, float y) const {
+    const float mn = fmax_nan_free(m, fmax_nan_free(x, y));
+    const float r = mn == -INFINITY ? 0.f : mn * c;  // all -inf so far: keep s = 0
+    s = fmaf(s, ex2_approx(fmaf(m, c, -r)), ex2_approx(fmaf(x, c, -r)) + ex2_approx(fmaf(y, c, -r)));
+    m = mn;
+  }
+  __device__ __forceinline__ void merge(float& m, float& s, int o) const {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mn = fmax_nan_free(m, om);
+    const float r = mn == -INFINITY ? 0.f : mn * c;
+    s = fmaf(s, ex2_approx(fmaf(m, c, -r)), os * ex2_approx(fmaf(om, c, -r)));
+    m = mn;
+  }
+  template <bool kMask>
+  __device__ __forceinline__ void add(float v0, float v1, float v2, float v3, int t0, int L0,
+                                      int L1) {
+    if (kMask) {
+      v0 = t0 < L0 ? v0 : -INFINITY;
+      v1 = t0 + 1 < L0 ? v1 : -INFINITY;
+      v2 = t0 < L1 ? v2 : -INFINITY;
+      v3 = t0 + 1 < L1 ? v3 : -INFINITY;
+    }
+    push2(m0, s0, v0, v1);
+    push2(m1, s1, v2, v3);
+  }
+  __device__ __forceinline__ void reduce() {
+    merge(m0, s0, 1);
+    merge(m0, s0, 2);
+    merge(m1, s1, 1);
+    merge(m1, s1, 2);
+  }
+  __device__ __forceinline__ float lse(float m, float s) const {
+    return m == -INFINITY ? m : (m * c + log2f(s)) * 0.6931471805599453f;
+  }
+  __device__ __forceinline__ float out0() const { return lse(m0, s0); }
+  __device__ __forceinline__ float out1() const { return lse(m1, s1); }
+};
 
 // ---------------------------------------------------------------------------
 // Query tiles in mma.sync A-fragment order.
@@ -275,10 +348,10 @@ struct BlockScorer;
 
 template <>
 struct BlockScorer<kBf16> {
-  template <bool kMask>
+  template <bool kMask, class Score>
   __device__ static void run(const QTile<kBf16>& qt, uint32_t stage, uint32_t /*scale_stage*/,
                              const float* /*scale_smem*/, int lane, int tbase, int L0, int L1,
-                             float qs0, float qs1, float& mx0, float& mx1) {
+                             float qs0, float qs1, Score& sc) {
     const int t = lane & 3;
     const int m = lane >> 3, rr = lane & 7;
 #pragma unroll 2
@@ -298,7 +371,7 @@ struct BlockScorer<kBf16> {
         mma_bf16_16816(acc, qt.a[2 * c + 1], b2, b3);
       }
       const int t0 = tbase + nt * 8 + 2 * t;
-      take<kMask>(mx0, mx1, acc[0], acc[1], acc[2], acc[3], t0, L0, L1);
+      sc.template add<kMask>(acc[0], acc[1], acc[2], acc[3], t0, L0, L1);
     }
     (void)qs0;
     (void)qs1;
@@ -307,10 +380,10 @@ struct BlockScorer<kBf16> {
 
 template <>
 struct BlockScorer<kFp8> {
-  template <bool kMask>
+  template <bool kMask, class Score>
   __device__ static void run(const QTile<kFp8>& qt, uint32_t stage, uint32_t /*scale_stage*/,
                              const float* scale_smem, int lane, int tbase, int L0, int L1,
-                             float qs0, float qs1, float& mx0, float& mx1) {
+                             float qs0, float qs1, Score& sc) {
     const int t = lane & 3;
     const int m = lane >> 3, rr = lane & 7;
 #pragma unroll 2
@@ -331,18 +404,18 @@ struct BlockScorer<kFp8> {
       const int jt = nt * 8 + 2 * t;  // token of acc[0] within the block
       const float2 ks = *reinterpret_cast<const float2*>(scale_smem + jt);
       const int t0 = tbase + jt;
-      take<kMask>(mx0, mx1, (acc[0] * qs0) * ks.x, (acc[1] * qs0) * ks.y, (acc[2] * qs1) * ks.x,
-                  (acc[3] * qs1) * ks.y, t0, L0, L1);
+      sc.template add<kMask>((acc[0] * qs0) * ks.x, (acc[1] * qs0) * ks.y, (acc[2] * qs1) * ks.x,
+                             (acc[3] * qs1) * ks.y, t0, L0, L1);
     }
   }
 };
 
 template <>
 struct BlockScorer<kNvfp4> {
-  template <bool kMask>
+  template <bool kMask, class Score>
   __device__ static void run(const QTile<kNvfp4>& qt, uint32_t stage, uint32_t scale_stage,
                              const float* /*scale_smem*/, int lane, int tbase, int L0, int L1,
-                             float /*qs0*/, float /*qs1*/, float& mx0, float& mx1) {
+                             float /*qs0*/, float /*qs1*/, Score& score) {
     const int g = lane >> 2, t = lane & 3;
     const int m = lane >> 3, rr = lane & 7;
     const uint32_t th = (uint32_t)(t >> 1);
@@ -380,7 +453,8 @@ struct BlockScorer<kNvfp4> {
         mma_f16_16816(acc, qt.a[2 * mm + 1], k2, k3);
       }
       const int t0 = tbase + nt * 8 + 2 * t;
-      take<kMask>(mx0, mx1, acc[0], acc[1], acc[2], acc[3], t0, L0, L1);
+      // raw sums of the rescaled query: the score applies qt.post_scale()
+      score.template add<kMask>(acc[0], acc[1], acc[2], acc[3], t0, L0, L1);
     }
   }
 };
@@ -455,7 +529,7 @@ __device__ __forceinline__ void issue_unit(const ScoreArgs& a, const CUtensorMap
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int KF>
+template <int KF, class Score>
 __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap payload_map) {
   using L = Layout<KF>;
@@ -474,10 +548,9 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t bar = sbase + L::kBarOff + warp * 8;  // this warp's stage barrier
-
   if (lane == 0) {
-    mbar_init(bar, 1);
+#pragma unroll
+    for (int d = 0; d < L::D; ++d) mbar_init(sbase + L::kBarOff + (warp * L::D + d) * 8, 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 0) prefetch_tensormap(&payload_map);
@@ -553,32 +626,45 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     return u;
   };
 
-  const uint32_t stage = sbase + L::kPayloadOff + warp * L::kStagePayload;
-  const uint32_t scale_stage = sbase + L::kScaleOff + warp * L::kStageScale;
-  const float* scale_smem = reinterpret_cast<const float*>(smem + L::kScaleOff + warp * L::kStageScale);
+  constexpr int D = L::D;
   const int g = lane >> 2, t = lane & 3;
   bool aborted = false;
-  uint32_t issued = 0;  // copies this warp has put into its stage
 
-  int cur = next_unit(), v_cur = 0, b_cur = 0;
-  if (cur >= 0) {
-    locate(gpre, V, cur, v_cur, b_cur);
-    const int pg = load_page(a, gpre, gslot, v_cur, b_cur, lane, cta_flags);
-    const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
-    if (lane == 0) issue_unit<KF>(a, &payload_map, sbase, warp, p0, p1);
-    ++issued;
+  // blocks in flight for this warp, oldest first: fv/fb = group and block
+  int fv[D], fb[D];
+  int nin = 0;
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    if (nin == d) {
+      const int u = next_unit();
+      if (u >= 0) {
+        locate(gpre, V, u, fv[d], fb[d]);
+        const int pg = load_page(a, gpre, gslot, fv[d], fb[d], lane, cta_flags);
+        const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
+        if (lane == 0) issue_unit<KF>(a, &payload_map, sbase, warp * D + d, p0, p1);
+        ++nin;
+      }
+    }
   }
-  int nxt = cur >= 0 ? next_unit() : -1, v_n = 0, b_n = 0, pg_n = -1;
+  // the block that goes out when the oldest one is scored (pages looked up early)
+  int nxt = nin == D ? next_unit() : -1, v_n = 0, b_n = 0, pg_n = -1;
   if (nxt >= 0) {
     locate(gpre, V, nxt, v_n, b_n);
     pg_n = load_page(a, gpre, gslot, v_n, b_n, lane, cta_flags);
   }
 
+  int k = 0;  // blocks scored by this warp
   int cur_v = -1;
   QTile<KF> qt;
   int L0 = 0, L1 = 0, row0 = -1, row1 = -1;
   float qs0 = 1.f, qs1 = 1.f;
-  while (cur >= 0) {
+  while (nin > 0) {
+    const int v_cur = fv[0], b_cur = fb[0];
+    const int sidx = warp * D + (k % D);
+    const uint32_t stage = sbase + L::kPayloadOff + sidx * L::kStagePayload;
+    const uint32_t scale_stage = sbase + L::kScaleOff + sidx * L::kStageScale;
+    const float* scale_smem = reinterpret_cast<const float*>(smem + L::kScaleOff + sidx * L::kStageScale);
+    const uint32_t bar = sbase + L::kBarOff + sidx * 8;
     // a new group's query tile is loaded while the block's keys are in flight
     if (v_cur != cur_v) {
       const Group gi = group_info(a, v_cur);
@@ -593,49 +679,46 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       }
       cur_v = v_cur;
     }
-    if (!mbar_wait_bounded(bar, (issued - 1) & 1)) {
+    if (!mbar_wait_bounded(bar, (k / D) & 1)) {
       if (lane == 0) atomicOr(cta_flags, kErrTimeout);
       aborted = true;
       break;
     }
     __syncwarp();
     const int tbase = b_cur * kBlock;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    Score score(qt.post_scale());
     // most blocks lie inside every live row: score them without the mask
     const bool whole = __all_sync(0xffffffffu, (row0 < 0 || tbase + kBlock <= L0) &&
                                                    (row1 < 0 || tbase + kBlock <= L1));
     if (whole)
       BlockScorer<KF>::template run<false>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
-                                           L1, qs0, qs1, mx0, mx1);
+                                           L1, qs0, qs1, score);
     else
       BlockScorer<KF>::template run<true>(qt, stage, scale_stage, scale_smem, lane, tbase, L0,
-                                          L1, qs0, qs1, mx0, mx1);
+                                          L1, qs0, qs1, score);
     // every lane's shared-memory reads of this stage are done; order them
     // before the asynchronous copies that overwrite it
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     const int p0 = __shfl_sync(0xffffffffu, pg_n, 0), p1 = __shfl_sync(0xffffffffu, pg_n, 1);
-    if (nxt >= 0) {
-      if (lane == 0) issue_unit<KF>(a, &payload_map, sbase, warp, p0, p1);
-      ++issued;
+    if (nxt >= 0 && lane == 0) issue_unit<KF>(a, &payload_map, sbase, sidx, p0, p1);
+    score.reduce();
+    if (t == 0) {
+      if (row0 >= 0 && tbase < L0) a.blockmax[(size_t)row0 * a.nb_cap + b_cur] = score.out0();
+      if (row1 >= 0 && tbase < L1) a.blockmax[(size_t)row1 * a.nb_cap + b_cur] = score.out1();
     }
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      mx0 = fmax_nan_free(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmax_nan_free(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    for (int d = 0; d + 1 < D; ++d) {
+      fv[d] = fv[d + 1];
+      fb[d] = fb[d + 1];
     }
-    if (KF == kNvfp4) {
-      mx0 *= qt.post_scale();
-      mx1 *= qt.post_scale();
+    fv[D - 1] = v_n;
+    fb[D - 1] = b_n;
+    ++k;
+    if (nxt < 0) {
+      --nin;
+      continue;
     }
-    if (t == 0) {
-      if (row0 >= 0 && tbase < L0) a.blockmax[(size_t)row0 * a.nb_cap + b_cur] = mx0;
-      if (row1 >= 0 && tbase < L1) a.blockmax[(size_t)row1 * a.nb_cap + b_cur] = mx1;
-    }
-    cur = nxt;
-    v_cur = v_n;
-    b_cur = b_n;
-    if (cur < 0) break;
     nxt = next_unit();
     pg_n = -1;
     if (nxt >= 0) {
@@ -643,8 +726,14 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       pg_n = load_page(a, gpre, gslot, v_n, b_n, lane, cta_flags);
     }
   }
-  // after a timeout, let this warp's copy still in flight land before exiting
-  if (aborted && lane == 0) (void)mbar_wait_bounded(bar, (issued - 1) & 1, 200000000ull);
+  // after a timeout, let this warp's copies still in flight land before exiting
+  if (aborted && lane == 0) {
+    for (int j = 0; j < nin; ++j) {
+      const int kk = k + j;
+      (void)mbar_wait_bounded(sbase + L::kBarOff + (warp * D + kk % D) * 8, (kk / D) & 1,
+                              200000000ull);
+    }
+  }
   // publish this CTA's flags (one byte per CTA, overwritten by every call, so no
   // clearing is needed between calls)
   __syncthreads();
@@ -656,7 +745,7 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
 
 std::atomic<int> g_grid_limit{0};
 
-template <int KF>
+template <int KF, class Score>
 cudaError_t launch_kf(const ScoreArgs& a, const CUtensorMap& map, cudaStream_t stream) {
   using L = Layout<KF>;
   int dev = 0;
@@ -665,14 +754,29 @@ cudaError_t launch_kf(const ScoreArgs& a, const CUtensorMap& map, cudaStream_t s
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(score_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(score_kernel<KF, Score>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            L::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int lim = g_grid_limit.load(std::memory_order_relaxed);
   int grid = (lim > 0 && lim < sms) ? lim : sms;
   if (grid > kMaxScoreCtas) grid = kMaxScoreCtas;
-  score_kernel<KF><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, map);
+  score_kernel<KF, Score><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, map);
   return cudaGetLastError();
+}
+
+template <class Score>
+cudaError_t launch_bs(int key_format, const ScoreArgs& args, const CUtensorMap& map,
+                      cudaStream_t stream) {
+  switch (key_format) {
+    case kBf16:
+      return launch_kf<kBf16, Score>(args, map, stream);
+    case kFp8:
+      return launch_kf<kFp8, Score>(args, map, stream);
+    case kNvfp4:
+      return launch_kf<kNvfp4, Score>(args, map, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -680,18 +784,10 @@ cudaError_t launch_kf(const ScoreArgs& a, const CUtensorMap& map, cudaStream_t s
 void set_grid_limit(int max_ctas) { g_grid_limit.store(max_ctas < 0 ? 0 : max_ctas); }
 int grid_limit() { return g_grid_limit.load(); }
 
-cudaError_t launch_score(int key_format, const ScoreArgs& args, const CUtensorMap& payload_map,
-                         cudaStream_t stream) {
-  switch (key_format) {
-    case kBf16:
-      return launch_kf<kBf16>(args, payload_map, stream);
-    case kFp8:
-      return launch_kf<kFp8>(args, payload_map, stream);
-    case kNvfp4:
-      return launch_kf<kNvfp4>(args, payload_map, stream);
-    default:
-      return cudaErrorInvalidValue;
-  }
+cudaError_t launch_score(int key_format, int block_score, const ScoreArgs& args,
+                         const CUtensorMap& payload_map, cudaStream_t stream) {
+  if (block_score == kBlockLse) return launch_bs<LseScore>(key_format, args, payload_map, stream);
+  return launch_bs<MaxScore>(key_format, args, payload_map, stream);
 }
 
 }  // namespace idx

@@ -27,7 +27,7 @@ def device_planes(batch, dev="cuda"):
 
 
 def run(batch, perrow=False, planes=None, dev="cuda", topk=None, init_blocks=None,
-        local_blocks=None, page_table=None):
+        local_blocks=None, page_table=None, block_score="max"):
     s = batch.spec
     topk = s.topk if topk is None else topk
     init_blocks = s.init_blocks if init_blocks is None else init_blocks
@@ -40,7 +40,11 @@ def run(batch, perrow=False, planes=None, dev="cuda", topk=None, init_blocks=Non
     out_ids = torch.full((R, M, topk), 7777, dtype=torch.int32, device=dev)
     out_sc = torch.full((R, M, topk), 7777.0, dtype=torch.float32, device=dev)
     ws = idx.alloc_workspace(R, s.packed_queries, s.gqa, int(pt.shape[1]), device=dev)
-    fn = idx.idx_score_topk_perrow if perrow else idx.idx_score_topk
+    if block_score == "lse":
+        assert not perrow
+        fn = idx.idx_score_topk_lse
+    else:
+        fn = idx.idx_score_topk_perrow if perrow else idx.idx_score_topk
     fn(q, q_scale, payload, scale, s.k_dtype, pt, batch.slot_ids.to(dev), batch.row_lens.to(dev),
        s.packed_queries, s.gqa, init_blocks, local_blocks, topk, out_ids, out_sc, ws)
     flags = idx.idx_workspace_errors(ws)

@@ -80,6 +80,56 @@ def test_small_parity(k_dtype, q_dtype, seed, P, G, lens, pads, init, local, top
     _check_all_rows(b, out, ref)
 
 
+LSE = []
+for k_dtype, q_dtype in [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3"), ("nvfp4", "bf16")]:
+    for seed, (P, G), lens, pads, init, local, topk in [
+        (111, (4, 4), (1, 9000), (2,), 1, 2, 16),
+        (112, (1, 16), (100, 6000), (), 2, 2, 8),
+        (113, (2, 3), (1, 4000), (), 1, 0, 12),
+    ]:
+        LSE.append(pytest.param(k_dtype, q_dtype, seed, P, G, lens, pads, init, local, topk,
+                                id=f"{k_dtype}-{seed}-P{P}G{G}"))
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype,seed,P,G,lens,pads,init,local,topk", LSE)
+def test_lse_block_score_parity(k_dtype, q_dtype, seed, P, G, lens, pads, init, local, topk):
+    """Log-sum-exp block score (sglang #45451, Accuracy Tests): every block's
+    score and every row's selection against the oracle's lse reading."""
+    spec = workloads.small_spec(f"l{seed}", seed, k_dtype, q_dtype, R=5, P=P, G=G,
+                                init_blocks=init, local_blocks=local, topk=topk, len_range=lens,
+                                pad_requests=pads)
+    b = workloads.make_batch(spec)
+    out = _gpu.run(b, block_score="lse")
+    ref = oracle.index.index_step(**oracle_kwargs(b), block_score="lse")
+    assert out.flags == 0
+    _check_blockmax(b, out, ref)
+    _check_all_rows(b, out, ref)
+
+
+def test_lse_bounds_the_max_on_device():
+    """On the same planes, max <= lse <= max + ln(tokens in the block) for
+    every block both variants score."""
+    spec = workloads.small_spec("lb", 121, "bf16", "bf16", R=4, len_range=(1, 6000), topk=16)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    mx = _gpu.run(b, planes=planes)
+    ls = _gpu.run(b, planes=planes, block_score="lse")
+    lens = b.row_lens.numpy().reshape(b.R, spec.packed_queries)
+    for r in range(b.R):
+        if not (0 <= int(b.slot_ids[r]) < b.page_table.shape[0]):
+            continue
+        for i in range(b.M):
+            L = int(lens[r, i // spec.gqa])
+            nb = (L + 127) // 128
+            if nb == 0:
+                continue
+            m = mx.blockmax[r * b.M + i, :nb].astype(np.float64)
+            l = ls.blockmax[r * b.M + i, :nb].astype(np.float64)
+            n = np.minimum(128, L - 128 * np.arange(nb))
+            assert np.all(l >= m - score_tol(m)), (r, i)
+            assert np.all(l <= m + np.log(n) + score_tol(m)), (r, i)
+
+
 @pytest.mark.parametrize("name", ["verify_bf16_4x32k", "verify_fp8_4x32k"])
 def test_verify_rows_4x4_ending_32767(name):
     """4 requests x 4 draft rows ending at tokens 32767..32770: one tile mixes
