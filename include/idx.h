@@ -38,7 +38,9 @@ extern "C" {
 #define IDX_PAGE_SIZE 64
 #define IDX_BLOCK_SIZE 128
 #define IDX_DIM 128
-#define IDX_MAX_PACKED_ROWS 16
+#define IDX_MAX_PACKED_ROWS 16        /* rows of one warp-MMA tile (P*G up to this) */
+#define IDX_WIDE_TILE_ROWS 128        /* rows of one tensor-core tile (P*G above 16) */
+#define IDX_MAX_ROWS_PER_REQUEST 32768 /* packed_queries * gqa of one request */
 #define IDX_MAX_TOPK 256
 #define IDX_WORKSPACE_HEADER_BYTES 1024
 #define IDX_MAX_REQUESTS 2048  /* per idx_score_topk call (draft rows per per-row call) */
@@ -130,9 +132,13 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  * Modifications; sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring for EAGLE
  * verify rows", Modifications 1).
  *
- * For request r, its P = packed_queries draft rows times G = gqa heads (P*G <= 16)
- * form one 16-row tile; tile row i is (draft row i / G, head i % G).  The tile is
- * dotted with the request's keys, read once per request up to the group's longest
+ * For request r, its P = packed_queries draft rows times G = gqa heads form its
+ * packed rows; row i is (draft row i / G, head i % G).  With P*G <= 16 the rows are
+ * one 16-row tile, dotted with the request's keys on the warp-level tensor-core MMA
+ * with the keys read once per request up to the group's longest row.  With P*G > 16
+ * (many draft rows, or a prefill chunk: P query tokens, each its own row length) the
+ * rows are cut into tiles of IDX_WIDE_TILE_ROWS, each dotted on the 5th-generation
+ * tensor cores (tcgen05) with the keys read once per tile up to the tile's longest
  * row.  Row i then keeps only tokens t < its own length, takes the max score of each
  * 128-token block, always keeps its first init_blocks and last local_blocks blocks
  * (from its own block count), and emits topk block ids with their scores.
@@ -166,8 +172,9 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  * blocks by descending score (ties to the lower id), then (-1, -inf) pads.  Scores are
  * raw q.k block maxima (fp8: code dot products times q_scale times the key's scale).
  * Asynchronous on stream; allocates nothing; capturable in a CUDA graph.
- * Host-side checks return IDX_ERR_INVALID (P*G outside [1,16], topk out of range,
- * init+local > topk, NULL pointers, R < 0 or > IDX_MAX_REQUESTS, n_slots or
+ * Host-side checks return IDX_ERR_INVALID (P*G outside [1, IDX_MAX_ROWS_PER_REQUEST],
+ * topk out of range, init+local > topk, NULL pointers, R < 0 or > IDX_MAX_REQUESTS,
+ * R * ceil(P*G / IDX_WIDE_TILE_ROWS) > IDX_MAX_REQUESTS when P*G > 16, n_slots or
  * max_pages < 1, workspace too
  * small or misaligned, num_pages < 1).  With R == 0 only the workspace is required
  * (its header is reset) and the per-request pointers may be NULL.

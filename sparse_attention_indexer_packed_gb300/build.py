@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libidx.so")
-SOURCES = ["idx_api.cu", "idx_score.cu", "idx_topk.cu", "idx_store.cu", "idx_noalloc.cu"]
+SOURCES = ["idx_api.cu", "idx_score.cu", "idx_wide.cu", "idx_topk.cu", "idx_store.cu", "idx_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-Xptxas", "-warn-spills"]

@@ -104,6 +104,35 @@ int make_payload_map(int dtype, const void* payload, int64_t num_pages, CUtensor
   return IDX_OK;
 }
 
+// Tensor map over the query rows [rows][128] for the 128-row tiles of the
+// tensor-core path: bf16 as two 64-column boxes, e4m3 as one 128-byte box, both
+// 128 rows high with the 128-byte swizzle the MMA operand descriptors expect.
+// Rows past the end read as zeros.
+int make_q_map(int q_dtype, const void* q, int64_t rows, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1];
+  cuuint32_t box[2] = {0, 128};
+  const cuuint32_t estride[2] = {1, 1};
+  CUtensorMapDataType dt;
+  if (q_dtype == IDX_BF16) {
+    dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    strides[0] = 256;
+    box[0] = 64;
+  } else {
+    dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    strides[0] = 128;
+    box[0] = 128;
+  }
+  CUresult r = fn(map, dt, 2, const_cast<void*>(q), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled (query rows) failed (%d)", (int)r);
+  return IDX_OK;
+}
+
 int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_scale, int q_dtype,
                     const void* k_payload, const void* k_scale, int k_dtype, int64_t num_pages,
                     const int32_t* page_table, int n_slots, int max_pages, const int32_t* slot_ids,
@@ -111,8 +140,19 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
                     int local_blocks, int topk, int32_t* out_ids, float* out_scores,
                     void* workspace, size_t workspace_bytes, void* stream) {
   if (R < 0) return fail(IDX_ERR_INVALID, "num_requests must be >= 0 (got %d)", R);
-  if (P < 1 || G < 1 || P * G > IDX_MAX_PACKED_ROWS)
-    return fail(IDX_ERR_INVALID, "packed_queries * gqa must be in [1, 16] (got %d x %d)", P, G);
+  if (P < 1 || G < 1 || (long long)P * G > IDX_MAX_ROWS_PER_REQUEST)
+    return fail(IDX_ERR_INVALID, "packed_queries * gqa must be in [1, %d] (got %d x %d)",
+                IDX_MAX_ROWS_PER_REQUEST, P, G);
+  if (perrow && G > IDX_MAX_PACKED_ROWS)
+    return fail(IDX_ERR_INVALID, "per-row scoring needs gqa <= %d (got %d)", IDX_MAX_PACKED_ROWS,
+                G);
+  const bool wide = !perrow && P * G > IDX_MAX_PACKED_ROWS;
+  const int tiles = (P * G + IDX_WIDE_TILE_ROWS - 1) / IDX_WIDE_TILE_ROWS;
+  if (wide && (long long)R * tiles > idx::kMaxGroups)
+    return fail(IDX_ERR_INVALID,
+                "at most %d request tiles per call (num_requests * ceil(packed_queries * gqa / "
+                "%d) = %lld)",
+                idx::kMaxGroups, IDX_WIDE_TILE_ROWS, (long long)R * tiles);
   if (topk < 1 || topk > IDX_MAX_TOPK)
     return fail(IDX_ERR_INVALID, "topk must be in [1, %d] (got %d)", IDX_MAX_TOPK, topk);
   if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > topk)
@@ -183,10 +223,17 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
   sa.G = G;
   sa.M = P * G;
   sa.perrow = perrow ? 1 : 0;
+  sa.tiles = tiles;
+  CUtensorMap qmap = map;
+  if (wide && k_dtype != IDX_NVFP4) {
+    rc = make_q_map(q_dtype, q, (int64_t)R * P * G, &qmap);
+    if (rc != IDX_OK) return rc;
+  }
   cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
   g_ev[0] = g_ev[1] = g_ev[2] = nullptr;
   if (ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
-  e = idx::launch_score(k_dtype, block_score, sa, map, st);
+  e = wide ? idx::launch_wide(k_dtype, block_score, sa, map, qmap, st)
+           : idx::launch_score(k_dtype, block_score, sa, map, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
   if (ev[1] && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
 

@@ -50,6 +50,7 @@ struct ScoreArgs {
   int n_slots, max_pages, nb_cap;
   int R, P, G, M;
   int perrow;                  // 0: groups are requests; 1: groups are draft rows
+  int tiles;                   // wide path: 128-row tiles per request (groups = R * tiles)
 };
 
 struct TopkArgs {
@@ -75,6 +76,11 @@ int grid_limit();
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_score(int key_format, int block_score, const ScoreArgs& args,
                          const CUtensorMap& payload_map, cudaStream_t stream);
+// Requests of more than 16 packed rows: 128-row tiles on tcgen05 (q_map: the
+// query rows [R*M][128] as bf16 or e4m3; unused for NVFP4 keys).
+cudaError_t launch_wide(int key_format, int block_score, const ScoreArgs& args,
+                        const CUtensorMap& payload_map, const CUtensorMap& q_map,
+                        cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& args, cudaStream_t stream);
 cudaError_t launch_store_nvfp4(const uint16_t* src, const int64_t* slot_mapping, int64_t num_tokens,
                                uint8_t* payload, uint8_t* scale, int64_t num_rows,

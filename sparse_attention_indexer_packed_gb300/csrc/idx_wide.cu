@@ -1,0 +1,679 @@
+// Block scores of wide requests -- more than 16 packed rows, e.g. many EAGLE
+// draft rows x heads, or a prefill chunk whose query tokens each end at their own
+// position -- on the 5th-generation tensor cores.
+//
+// The rows of a request are cut into tiles of up to 128 (tile tau holds rows
+// [128 tau, 128 tau + 128)); each tile is one "group" that streams the request's
+// keys once.  A 128-row x 128-token x 128-dim product is one tcgen05.mma chain
+// (M = 128, N = 128) accumulating in fp32 in tensor memory, so the dot work of
+// the pages' per-request dot tile (sglang #45451, Modifications: the draft rows of
+// a request share one dot tile against its index K) is done for 128 rows at a
+// time instead of 16.  Each row keeps its own length mask and its block max (or
+// log-sum-exp), exactly as the 16-row path does; the oracle's per-row definition
+// is the same for both.
+//
+// Roles inside a CTA (one CTA per SM, persistent over a contiguous range of
+// blocks of the flattened (group, block) list):
+//   warp 0      TMA producer: the group's query tile (bf16 / e4m3) and each
+//               block's two key pages (+ their scales) into a ring of stages;
+//   warp 1      allocates 256 TMEM columns (two 128-column accumulators); lane 0
+//               issues the MMAs of a block and commits them to mbarriers;
+//   warps 2..5  epilogue: thread = tile row; tcgen05.ld of its 128 scores, the
+//               row's mask and block score, one workspace write per row;
+//   warps 6..9  (NVFP4 keys) decode a block's e2m1 codes x E4M3 group scales into
+//               an f16 operand tile (ROCm/ATOM #2745: the products are exact);
+//               the epilogue warps also convert the bf16 query tile to f16 with a
+//               per-row power-of-two scale, undone on the result.
+// Every wait is bounded; a timeout sets IDX_DEVERR_TIMEOUT and the CTA winds down
+// (copies in flight are waited for, TMEM is freed).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "idx_internal.cuh"
+#include "idx_ptx.cuh"
+#include "idx_tc.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kWRows = 128;     // tile rows (MMA M)
+constexpr int kTmemCols = 256;  // two fp32 accumulators of 128 columns
+constexpr unsigned int kErrBadPage = 1u;  // IDX_DEVERR_BAD_PAGE
+constexpr unsigned int kErrTimeout = 2u;  // IDX_DEVERR_TIMEOUT
+constexpr unsigned int kErrLenClamped = 4u;  // IDX_DEVERR_LEN_CLAMPED
+
+template <int KF>
+struct WCfg;
+template <>
+struct WCfg<kBf16> {
+  static constexpr int kQBytes = 32768;     // 128 rows x 256 B: two 16 KB K-halves
+  static constexpr int kStageBytes = 32768; // 128 tokens x 256 B: two 16 KB K-halves
+  static constexpr int kPagePayload = 16384;
+  static constexpr int kPageScale = 0;
+  static constexpr int kStages = 4;
+  static constexpr int kDecStages = 0;
+  static constexpr int kDecWarps = 0;
+  static constexpr uint32_t kIdesc = instr_desc(1u, 128, 128);  // bf16 x bf16
+};
+template <>
+struct WCfg<kFp8> {
+  static constexpr int kQBytes = 16384;     // 128 rows x 128 B
+  static constexpr int kStageBytes = 16384; // 128 tokens x 128 B
+  static constexpr int kPagePayload = 8192;
+  static constexpr int kPageScale = 256;    // 64 fp32
+  static constexpr int kStages = 6;
+  static constexpr int kDecStages = 0;
+  static constexpr int kDecWarps = 0;
+  static constexpr uint32_t kIdesc = instr_desc(0u, 128, 128);  // e4m3 x e4m3
+};
+template <>
+struct WCfg<kNvfp4> {
+  static constexpr int kQBytes = 32768;     // f16 query tile
+  static constexpr int kStageBytes = 8192;  // raw codes of 128 tokens (64 B each)
+  static constexpr int kPagePayload = 4096;
+  static constexpr int kPageScale = 512;    // 64 x 8 E4M3 bytes
+  static constexpr int kStages = 4;
+  static constexpr int kDecStages = 3;      // decoded f16 tiles, 32 KB each
+  static constexpr int kDecWarps = 4;
+  static constexpr uint32_t kIdesc = instr_desc(0u, 128, 128);  // f16 x f16
+};
+
+template <int KF>
+struct WLayout {
+  using C = WCfg<KF>;
+  static constexpr int S = C::kStages;
+  static constexpr int SD = C::kDecStages;
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = kQOff + C::kQBytes;
+  static constexpr int kDecOff = kStageOff + S * C::kStageBytes;
+  static constexpr int kScaleOff = kDecOff + SD * 32768;
+  static constexpr int kBarOff = kScaleOff + S * 2 * C::kPageScale;
+  // full[S] empty[S] dfull[SD] dempty[SD] afull[2] aempty[2] qfull qempty done
+  static constexpr int kNumBars = 2 * S + 2 * SD + 7;
+  static constexpr int kCtlOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
+  static constexpr int kGroupOff = kCtlOff + 64;
+  static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
+  static constexpr int kSmemBytes = kBytes + 1024;
+  static constexpr int kWarps = 6 + C::kDecWarps;
+  static constexpr int kThreads = 32 * kWarps;
+  static_assert(kStageOff % 1024 == 0 && kDecOff % 1024 == 0, "operand tiles 1024-aligned");
+  static_assert(C::kStageBytes % 1024 == 0, "stages 1024-aligned");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+  __device__ static uint32_t full(uint32_t sb, int s) { return sb + kBarOff + 8 * s; }
+  __device__ static uint32_t empty(uint32_t sb, int s) { return sb + kBarOff + 8 * (S + s); }
+  __device__ static uint32_t dfull(uint32_t sb, int d) { return sb + kBarOff + 8 * (2 * S + d); }
+  __device__ static uint32_t dempty(uint32_t sb, int d) {
+    return sb + kBarOff + 8 * (2 * S + SD + d);
+  }
+  __device__ static uint32_t afull(uint32_t sb, int j) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + j);
+  }
+  __device__ static uint32_t aempty(uint32_t sb, int j) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 + j);
+  }
+  __device__ static uint32_t qfull(uint32_t sb) { return sb + kBarOff + 8 * (2 * S + 2 * SD + 4); }
+  __device__ static uint32_t qempty(uint32_t sb) { return sb + kBarOff + 8 * (2 * S + 2 * SD + 5); }
+  __device__ static uint32_t done(uint32_t sb) { return sb + kBarOff + 8 * (2 * S + 2 * SD + 6); }
+};
+
+__device__ __forceinline__ float fmax_nf(float a, float b) { return a > b ? a : b; }
+
+// Geometry of wide group v = (request r, tile tau).
+struct WGroup {
+  int r, row0, nrows, base_row, slot, extent, nbk;
+};
+
+__device__ WGroup wgroup_info(const ScoreArgs& a, int v) {
+  WGroup g;
+  g.r = v / a.tiles;
+  g.row0 = (v - g.r * a.tiles) * kWRows;
+  g.nrows = min(kWRows, a.M - g.row0);
+  g.base_row = g.r * a.M + g.row0;
+  g.slot = __ldg(a.slot_ids + g.r);
+  const bool pad = g.slot < 0 || g.slot >= a.n_slots;
+  int ext = 0;
+  const int j0 = g.row0 / a.G, j1 = (g.row0 + g.nrows - 1) / a.G;
+  for (int j = j0; j <= j1; ++j) ext = max(ext, __ldg(a.row_lens + g.r * a.P + j));
+  g.extent = min(ext, a.max_pages * kPage);
+  g.nbk = (pad || g.extent <= 0) ? 0 : (g.extent + kBlock - 1) / kBlock;
+  return g;
+}
+
+__device__ __forceinline__ void wlocate(const int* gpre, int V, int u, int& v, int& b) {
+  int lo = 0, hi = V - 1;  // largest v with gpre[v] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (gpre[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  v = lo;
+  b = u - gpre[lo];
+}
+
+// Page ids of block b of group v for lanes 0 and 1 (-1: no second page,
+// -2: bad page id, not read).
+__device__ __forceinline__ int wload_page(const ScoreArgs& a, const int* gpre, const int* gslot,
+                                          int v, int b, int lane, unsigned int* flags) {
+  int p = -1;
+  if (lane < 2) {
+    const int word = gslot[v];
+    const int slot = word & 0x7fffffff;
+    const bool last = b == gpre[v + 1] - gpre[v] - 1;
+    const bool want = lane == 0 || !(last && word < 0);
+    if (want) {
+      p = __ldg(a.page_table + (size_t)slot * a.max_pages + 2 * b + lane);
+      if (p < 0 || p >= a.num_pages) {
+        atomicOr(flags, kErrBadPage);
+        p = -2;
+      }
+    }
+  }
+  return p;
+}
+
+// Per-thread row scores over one block, fed 32 columns at a time.
+struct RowMax {
+  float m = -INFINITY;
+  float post;
+  __device__ __forceinline__ explicit RowMax(float post_scale) : post(post_scale) {}
+  template <bool kMask>
+  __device__ __forceinline__ void add32(const float (&x)[32], int t0, int L) {
+    float p = -INFINITY, q = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+      if (!kMask || t0 + k < L) p = fmax_nf(p, x[k]);
+      if (!kMask || t0 + k + 1 < L) q = fmax_nf(q, x[k + 1]);
+    }
+    m = fmax_nf(m, fmax_nf(p, q));
+  }
+  __device__ __forceinline__ float out() const { return m * post; }
+};
+
+// ln sum exp over the row's valid tokens of the block, kept as the running max
+// m of the raw sums and sum 2^((x - m) c), c = post * log2(e).
+struct RowLse {
+  float m = -INFINITY, s = 0.f;
+  float c;
+  __device__ __forceinline__ explicit RowLse(float post_scale)
+      : c(post_scale * 1.4426950408889634f) {}
+  template <bool kMask>
+  __device__ __forceinline__ void add32(const float (&x)[32], int t0, int L) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (!kMask || t0 + k < L) mx = fmax_nf(mx, x[k]);
+    const float mn = fmax_nf(m, mx);
+    const float r = mn == -INFINITY ? 0.f : mn * c;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+      if (!kMask || t0 + k < L) acc0 += ex2_approx(fmaf(x[k], c, -r));
+      if (!kMask || t0 + k + 1 < L) acc1 += ex2_approx(fmaf(x[k + 1], c, -r));
+    }
+    s = fmaf(s, ex2_approx(fmaf(m, c, -r)), acc0 + acc1);
+    m = mn;
+  }
+  __device__ __forceinline__ float out() const {
+    return m == -INFINITY ? m : (m * c + log2f(s)) * 0.6931471805599453f;
+  }
+};
+
+// Byte address of 16-byte chunk c (0..15) of row i in a 128-row x 256-byte
+// operand tile stored as two 128-byte-swizzled K-halves of 16 KB.
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int i, int c) {
+  const int h = c >> 3, cc = c & 7;
+  return tile + (uint32_t)(h * 16384 + (i >> 3) * 1024 + (i & 7) * 128 + ((cc ^ (i & 7)) << 4));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// f16 query tile for NVFP4 keys: row i of the tile (one thread) is rescaled by
+// 2^qexp so its largest magnitude lies in [2^14, 2^15) and stored as f16; every
+// element within 2^-24 of that maximum is exact.  Returns 2^-qexp.
+__device__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i, int base_row,
+                               int nrows) {
+  const bool valid = i < nrows;
+  const uint4* src = reinterpret_cast<const uint4*>(a.q + (size_t)(base_row + i) * 256);
+  float amax = 0.f;
+  if (valid) {
+#pragma unroll 4
+    for (int c = 0; c < 16; ++c) {
+      const uint4 u = __ldg(src + c);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[e] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[e] & 0xffff0000u)));
+      }
+    }
+  }
+  int qexp = 0;
+  if (amax > 0.f) qexp = 14 - (((__float_as_uint(amax) >> 23) & 0xff) - 127);
+  qexp = max(-100, min(100, qexp));
+  const float up = ldexpf(1.f, qexp);
+#pragma unroll 4
+  for (int c = 0; c < 16; ++c) {
+    uint32_t o[4] = {0u, 0u, 0u, 0u};
+    if (valid) {
+      const uint4 u = __ldg(src + c);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __half2 h = __floats2half2_rn(__uint_as_float(w[e] << 16) * up,
+                                      __uint_as_float(w[e] & 0xffff0000u) * up);
+        o[e] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+    st_shared_v4(sw128_chunk(qtile, i, c), o[0], o[1], o[2], o[3]);
+  }
+  return ldexpf(1.f, -qexp);
+}
+
+// Decode token n (0..127) of a raw NVFP4 stage into the f16 operand tile.
+// Raw payload: page pp = n / 64 at pp * 4096, row n % 64 at 64 B with the TMA
+// 64-byte swizzle (16-byte chunk m stored at m ^ ((row >> 1) & 3)); scales: page
+// pp at pp * 512, 8 bytes per token.
+__device__ __forceinline__ void decode_token(uint32_t raw, uint32_t rscale, uint32_t dec, int n) {
+  const int pp = n >> 6, nn = n & 63;
+  uint32_t s_lo, s_hi;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+               : "=r"(s_lo), "=r"(s_hi)
+               : "r"(rscale + (uint32_t)(pp * 512 + nn * 8)));
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(raw + (uint32_t)(pp * 4096 + nn * 64 + (((m ^ ((nn >> 1) & 3)) & 3) << 4))));
+    // elements 32m .. 32m+31: groups 2m (words 0, 1) and 2m+1 (words 2, 3)
+#pragma unroll
+    for (int hg = 0; hg < 2; ++hg) {
+      const int grp = 2 * m + hg;
+      const uint32_t sb = ((grp < 4 ? s_lo : s_hi) >> (8 * (grp & 3))) & 0xffu;
+      uint32_t sc, unused;
+      e4m3x4_to_f16x2x2(sb | (sb << 8), sc, unused);  // {scale, scale}
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int e = 2 * hg + e2;
+        uint32_t f[4];
+        e2m1x8_to_f16x2x4(w[e], f);
+        st_shared_v4(sw128_chunk(dec, n, 4 * m + e), hmul2_f16(f[0], sc), hmul2_f16(f[1], sc),
+                     hmul2_f16(f[2], sc), hmul2_f16(f[3], sc));
+      }
+    }
+  }
+}
+
+template <int KF, class RowScore>
+__global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
+    wide_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap qmap) {
+  using L = WLayout<KF>;
+  using C = WCfg<KF>;
+  constexpr int S = L::S;
+  constexpr int SD = L::SD;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  volatile int* ctl = reinterpret_cast<volatile int*>(smem + L::kCtlOff);
+  // ctl[0] = units of the call, ctl[1] = TMEM base, ctl[4] = device error flags
+  unsigned int* cta_flags = reinterpret_cast<unsigned int*>(smem + L::kCtlOff) + 4;
+  int* gpre = reinterpret_cast<int*>(smem + L::kGroupOff);
+  int* gslot = gpre + kMaxGroups + 1;
+  const uint32_t qtile = sb + L::kQOff;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(L::full(sb, s), 1);
+      // who frees a raw stage: the MMA (bf16), the MMA and the four epilogue
+      // warps that read its key scales (fp8), the four decoder warps (NVFP4)
+      mbar_init(L::empty(sb, s), KF == kBf16 ? 1 : (KF == kFp8 ? 5 : 4));
+    }
+    for (int d = 0; d < SD; ++d) {
+      mbar_init(L::dfull(sb, d), C::kDecWarps);
+      mbar_init(L::dempty(sb, d), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(L::afull(sb, j), 1);
+      mbar_init(L::aempty(sb, j), 4);
+    }
+    mbar_init(L::qfull(sb), KF == kNvfp4 ? 4 : 1);
+    mbar_init(L::qempty(sb), 1);
+    mbar_init(L::done(sb), 1);
+    fence_barrier_init();
+    prefetch_tensormap(&kmap);
+    if (KF != kNvfp4) prefetch_tensormap(&qmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + L::kCtlOff + 4, kTmemCols);
+    tmem_relinquish();
+  }
+
+  // ---- group table: block prefix sums and slots of every (request, tile) ----
+  const int V = a.R * a.tiles;
+  if (warp == 0) {
+    int run = 0;
+    bool clamped = false;
+    for (int v0 = 0; v0 < V; v0 += 32) {
+      const int v = v0 + lane;
+      int nbk = 0, word = 0;
+      if (v < V) {
+        const WGroup gi = wgroup_info(a, v);
+        nbk = gi.nbk;
+        const int rem = gi.extent - (nbk - 1) * kBlock;
+        word = (nbk > 0 ? gi.slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
+        if (blockIdx.x == 0 && gi.row0 == 0 && gi.slot >= 0 && gi.slot < a.n_slots)
+          for (int j = 0; j < a.P; ++j)
+            clamped |= __ldg(a.row_lens + gi.r * a.P + j) > a.max_pages * kPage;
+      }
+      int incl = nbk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (v < V) {
+        gpre[v] = run + incl - nbk;
+        gslot[v] = word;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    clamped = __any_sync(0xffffffffu, clamped);
+    if (lane == 0) {
+      gpre[V] = run;
+      ctl[0] = run;
+      *cta_flags = clamped ? kErrLenClamped : 0u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int U = ctl[0];
+  const uint32_t tmem = (uint32_t)ctl[1];
+  const int u0 = (int)((long long)U * blockIdx.x / gridDim.x);
+  const int u1 = (int)((long long)U * (blockIdx.x + 1) / gridDim.x);
+
+  if (warp == 0) {
+    // ======================= producer =======================
+    int prev_v = -1, nq = 0, i = 0;
+    bool ok = true;
+    for (int u = u0; u < u1 && ok; ++u, ++i) {
+      int v, b;
+      wlocate(gpre, V, u, v, b);
+      if (v != prev_v) {
+        if (KF != kNvfp4 && lane == 0) {
+          // the previous tile's MMAs must be done with the query tile
+          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
+          if (ok) {
+            const int r = v / a.tiles;
+            const int base_row = r * a.M + (v - r * a.tiles) * kWRows;
+            mbar_arrive_expect_tx(L::qfull(sb), C::kQBytes);
+            if (KF == kBf16) {
+              tma_load_2d(qtile, &qmap, 0, base_row, L::qfull(sb));
+              tma_load_2d(qtile + 16384, &qmap, 64, base_row, L::qfull(sb));
+            } else {
+              tma_load_2d(qtile, &qmap, 0, base_row, L::qfull(sb));
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++nq;
+        prev_v = v;
+      }
+      const int s = i % S;
+      if (lane == 0 && i >= S && !mbar_wait_bounded(L::empty(sb, s), ((i / S) - 1) & 1)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const int pg = wload_page(a, gpre, gslot, v, b, lane, cta_flags);
+      const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
+      if (lane == 0) {
+        uint32_t tx = 0;
+        if (p0 >= 0) tx += C::kPagePayload + C::kPageScale;
+        if (p1 >= 0) tx += C::kPagePayload + C::kPageScale;
+        const uint32_t fb = L::full(sb, s);
+        mbar_arrive_expect_tx(fb, tx);
+        const uint32_t dst = sb + L::kStageOff + s * C::kStageBytes;
+        const uint32_t sdst = sb + L::kScaleOff + s * 2 * C::kPageScale;
+        const int pgs[2] = {p0, p1};
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          if (pgs[pp] < 0) continue;
+          const int y = pgs[pp] * kPage;
+          if (KF == kBf16) {
+            tma_load_2d(dst + pp * 8192, &kmap, 0, y, fb);
+            tma_load_2d(dst + 16384 + pp * 8192, &kmap, 64, y, fb);
+          } else {
+            tma_load_2d(dst + pp * C::kPagePayload, &kmap, 0, y, fb);
+            bulk_load(sdst + pp * C::kPageScale, a.k_scale + (size_t)pgs[pp] * C::kPageScale,
+                      C::kPageScale, fb);
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(cta_flags, kErrTimeout);
+        // let the copies still in flight land before the CTA can exit
+        for (int k = max(0, i - S); k < i; ++k)
+          (void)mbar_wait_bounded(L::full(sb, k % S), (k / S) & 1, 200000000ull);
+        if (KF != kNvfp4 && nq > 0) (void)mbar_wait_bounded(L::qfull(sb), (nq - 1) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      int prev_v = -1, nq = 0, i = 0;
+      bool ok = true;
+      int v = 0, b = 0;
+      if (u0 < u1) wlocate(gpre, V, u0, v, b);
+      for (int u = u0; u < u1; ++u, ++i) {
+        if (v != prev_v) {
+          if (!mbar_wait_bounded(L::qfull(sb), nq & 1)) { ok = false; break; }
+          ++nq;
+          prev_v = v;
+        }
+        const int s = i % S;
+        uint32_t opnd;
+        if constexpr (KF == kNvfp4) {
+          const int d = i % SD;
+          if (!mbar_wait_bounded(L::dfull(sb, d), (i / SD) & 1)) { ok = false; break; }
+          opnd = sb + L::kDecOff + d * 32768;
+        } else {
+          if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1)) { ok = false; break; }
+          opnd = sb + L::kStageOff + s * C::kStageBytes;
+        }
+        const int j = i & 1;
+        if (i >= 2 && !mbar_wait_bounded(L::aempty(sb, j), ((i >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(j * 128);
+        if (KF == kFp8) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc_mma_f8(d_tmem, desc_kmajor_sw128(qtile + ks * 32), desc_kmajor_sw128(opnd + ks * 32),
+                      C::kIdesc, ks > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
+            tc_mma_f16(d_tmem, desc_kmajor_sw128(qtile + off), desc_kmajor_sw128(opnd + off),
+                       C::kIdesc, ks > 0 ? 1u : 0u);
+          }
+        }
+        if constexpr (KF == kNvfp4) tc_commit(L::dempty(sb, i % SD));
+        else tc_commit(L::empty(sb, s));
+        tc_commit(L::afull(sb, j));
+        int vn = -1, bn = 0;
+        if (u + 1 < u1) wlocate(gpre, V, u + 1, vn, bn);
+        if (vn != v) tc_commit(L::qempty(sb));  // last block of this tile
+        v = vn;
+        b = bn;
+      }
+      if (!ok) atomicOr(cta_flags, kErrTimeout);
+      // every MMA issued has completed before TMEM is released
+      tc_commit(L::done(sb));
+      (void)mbar_wait_bounded(L::done(sb), 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ======================= epilogue =======================
+    const int quarter = warp & 3;
+    const int ti = quarter * 32 + lane;  // tile row of this thread
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    int prev_v = -1, nq = 0, i = 0;
+    int Lrow = 0, out_row = -1;
+    float post = 1.f, qs = 0.f;
+    bool ok = true;
+    for (int u = u0; u < u1; ++u, ++i) {
+      int v, b;
+      wlocate(gpre, V, u, v, b);
+      if (v != prev_v) {
+        const WGroup gi = wgroup_info(a, v);
+        const bool live = ti < gi.nrows && gi.nbk > 0;
+        out_row = live ? gi.base_row + ti : -1;
+        Lrow = live ? min(__ldg(a.row_lens + gi.r * a.P + (gi.row0 + ti) / a.G),
+                          a.max_pages * kPage)
+                    : 0;
+        if (KF == kFp8) qs = live ? __ldg(a.q_scale + out_row) : 0.f;
+        if (KF == kNvfp4) {
+          // every MMA of the previous tile has completed (its last block's
+          // accumulator was waited for below), so the query tile is free
+          post = convert_q_row(a, qtile, ti, gi.base_row, gi.nrows);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(L::qfull(sb));
+        }
+        ++nq;
+        prev_v = v;
+      }
+      const int j = i & 1;
+      if (!mbar_wait_bounded(L::afull(sb, j), (i >> 1) & 1)) ok = false;
+      // the key scales this warp reads were written by the copy engine: observe
+      // their arrival itself (already complete, since the MMA waited for it)
+      if (KF == kFp8 && ok && !mbar_wait_bounded(L::full(sb, i % S), (i / S) & 1)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const int tbase = b * kBlock;
+      const float* ks = reinterpret_cast<const float*>(smem + L::kScaleOff + (i % S) * 2 * C::kPageScale);
+      RowScore sc(post);
+      const bool whole = tbase + kBlock <= Lrow;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t raw[32];
+        __syncwarp();
+        tc_ld_32cols(trow + (uint32_t)(j * 128 + c4 * 32), raw);
+        tc_wait_ld();
+        float x[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          x[k] = __uint_as_float(raw[k]);
+          if (KF == kFp8) x[k] = (x[k] * qs) * ks[c4 * 32 + k];
+        }
+        if (whole) sc.template add32<false>(x, tbase + c4 * 32, Lrow);
+        else sc.template add32<true>(x, tbase + c4 * 32, Lrow);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(L::aempty(sb, j));
+        if (KF == kFp8) mbar_arrive(L::empty(sb, i % S));
+      }
+      if (out_row >= 0 && tbase < Lrow) a.blockmax[(size_t)out_row * a.nb_cap + b] = sc.out();
+    }
+    if (!ok && lane == 0) atomicOr(cta_flags, kErrTimeout);
+  } else if constexpr (KF == kNvfp4) {
+    // ======================= NVFP4 decoders =======================
+    const int n = (warp - 6) * 32 + lane;  // token of the block
+    bool ok = true;
+    int i = 0;
+    for (int u = u0; u < u1; ++u, ++i) {
+      const int s = i % S, d = i % SD;
+      if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1)) ok = false;
+      if (ok && i >= SD && !mbar_wait_bounded(L::dempty(sb, d), ((i / SD) - 1) & 1)) ok = false;
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      decode_token(sb + L::kStageOff + s * C::kStageBytes, sb + L::kScaleOff + s * 2 * C::kPageScale,
+                   sb + L::kDecOff + d * 32768, n);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(L::dfull(sb, d));
+        mbar_arrive(L::empty(sb, s));
+      }
+    }
+    if (!ok && lane == 0) atomicOr(cta_flags, kErrTimeout);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    a.err_bytes[blockIdx.x] = (uint8_t)*cta_flags;
+    if (blockIdx.x == 0) *a.err_count = gridDim.x;
+  }
+}
+
+template <int KF, class RowScore>
+cudaError_t launch_wide_kf(const ScoreArgs& a, const CUtensorMap& kmap, const CUtensorMap& qmap,
+                           cudaStream_t stream) {
+  using L = WLayout<KF>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(wide_kernel<KF, RowScore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int lim = grid_limit();
+  int grid = (lim > 0 && lim < sms) ? lim : sms;
+  if (grid > kMaxScoreCtas) grid = kMaxScoreCtas;
+  wide_kernel<KF, RowScore><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, kmap, qmap);
+  return cudaGetLastError();
+}
+
+template <class RowScore>
+cudaError_t launch_wide_bs(int key_format, const ScoreArgs& a, const CUtensorMap& kmap,
+                           const CUtensorMap& qmap, cudaStream_t stream) {
+  switch (key_format) {
+    case kBf16:
+      return launch_wide_kf<kBf16, RowScore>(a, kmap, qmap, stream);
+    case kFp8:
+      return launch_wide_kf<kFp8, RowScore>(a, kmap, qmap, stream);
+    case kNvfp4:
+      return launch_wide_kf<kNvfp4, RowScore>(a, kmap, qmap, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wide(int key_format, int block_score, const ScoreArgs& args,
+                        const CUtensorMap& payload_map, const CUtensorMap& q_map,
+                        cudaStream_t stream) {
+  if (block_score == kBlockLse)
+    return launch_wide_bs<RowLse>(key_format, args, payload_map, q_map, stream);
+  return launch_wide_bs<RowMax>(key_format, args, payload_map, q_map, stream);
+}
+
+}  // namespace idx

@@ -62,7 +62,8 @@ def _call(L, **over):
 
 
 @pytest.mark.parametrize("over,status", [
-    (dict(P=5, G=4), -1),                 # more than 16 packed rows
+    (dict(P=200, G=200), -1),             # more than IDX_MAX_ROWS_PER_REQUEST rows
+    (dict(R=17, P=128, G=128), -1),       # 17 x 128 tensor-core tiles > 2048 per call
     (dict(P=0), -1),
     (dict(topk=0), -1),
     (dict(topk=257), -1),
