@@ -37,12 +37,20 @@ DEFAULT_WORKLOAD = "bf16_16x131k"
 PUBLISHED_US = {"bf16_16x131k": 119.1, "fp8_16x131k": 87.4}   # packed kernel, one GB300 rank
 BYTES_PER_TOKEN = {"bf16": 256, "fp8_e4m3": 132, "nvfp4": 72}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+L2_BYTES = 129 * 1024 * 1024
+L2_FLUSH_BYTES = 256 * 1024 * 1024
 SCORE_SOURCES = ["idx_score.cu", "idx_ptx.cuh", "idx_internal.cuh"]
+WIDE_SOURCES = ["idx_wide.cu", "idx_tc.cuh", "idx_ptx.cuh", "idx_internal.cuh"]
 
 
-def kernel_sha() -> str:
+def is_wide(spec) -> bool:
+    """More than 16 packed rows: the 128-row tensor-core tiles."""
+    return spec.packed_queries * spec.gqa > 16
+
+
+def kernel_sha(wide: bool = False) -> str:
     h = hashlib.sha256()
-    for f in SCORE_SOURCES:
+    for f in (WIDE_SOURCES if wide else SCORE_SOURCES):
         with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -56,6 +64,22 @@ def measured_peak():
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
     except Exception:
         return 6800.0, "fallback 6.8 TB/s"
+
+
+def measured_tensor_peak(k_dtype: str):
+    """Dense tensor-core peak in TFLOP/s for the MMA's input type: the measured
+    cuBLAS bf16 burst figure (f16 runs at the bf16 rate; e4m3 at twice it, the
+    nominal 4.5 / 2.25 PFLOP/s ratio)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            bf16 = float(json.load(fh)["bf16_tflops"])
+        src = "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 burst)"
+    except Exception:
+        bf16, src = 1900.0, "fallback 1.9 PFLOP/s bf16"
+    if k_dtype == "fp8_e4m3":
+        return 2.0 * bf16, src + " x 2 (e4m3 / bf16 nominal ratio)"
+    return bf16, src + (" (f16 operands: same rate)" if k_dtype == "nvfp4" else "")
 
 
 def algorithmic_bytes(batch) -> dict:
@@ -77,7 +101,17 @@ def algorithmic_bytes(batch) -> dict:
             L = int(batch.row_lens[r, j])
             bm += s.gqa * max(0, (L + 127) // 128) * 4
     out = batch.R * batch.M * s.topk * 8
-    return {"score": k_bytes + q_bytes + meta + bm, "keys": k_bytes, "topk": bm + out}
+    # useful multiply-adds: every row against every key inside its own length
+    flops = 0
+    for r in range(batch.R):
+        if lens[r] == 0:
+            continue
+        for j in range(s.packed_queries):
+            flops += s.gqa * max(0, int(batch.row_lens[r, j])) * 128 * 2
+    # per request the tensor-core path re-reads the keys once per 128-row tile
+    tiles = -(-batch.M // 128) if batch.M > 16 else 1
+    return {"score": k_bytes + q_bytes + meta + bm, "keys": k_bytes, "topk": bm + out,
+            "flops": flops, "key_reads_per_request": tiles}
 
 
 class ClockSampler:
@@ -242,20 +276,39 @@ def run_ours(args):
     # ---- timed region 1: K steps exactly as a caller runs them ----------------
     # (no events between the score and top-k launches: an event there stops the
     # top-k kernel's launch from overlapping the score kernel's tail)
+    # inputs that fit in L2 (129 MB) get it flushed before every step (a 256 MB
+    # write, outside each step's own pair of events); larger inputs stream
+    # through it anyway and run back to back
+    in_bytes = (payload.numel() + (0 if scale is None else scale.numel()) +
+                q.numel() * q.element_size())
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) \
+        if in_bytes < 2 * L2_BYTES else None
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
     barrier(ws_n)
     torch.cuda.synchronize(dev)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
+    if flush_buf is None:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        run_ms = t0.elapsed_time(t1)
+    else:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        for a_ev, b_ev in pairs:
+            flush_buf.fill_(1)
+            a_ev.record(stream)
+            step()
+            b_ev.record(stream)
+        torch.cuda.synchronize(dev)
+        run_ms = sum(a_ev.elapsed_time(b_ev) for a_ev, b_ev in pairs)
     barrier(ws_n)
-    total_ms = max_over_ranks(t0.elapsed_time(t1), ws_n, dev)
+    total_ms = max_over_ranks(run_ms, ws_n, dev)
 
     # ---- timed region 2: the same K steps with CUDA events recorded by the
     # library on the launching stream around each kernel (per-kernel durations)
@@ -271,12 +324,16 @@ def run_ours(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for k in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(1)
         step(evs[k])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(ws_n)
     clocks = sampler.stop()
-    evented_ms = max_over_ranks(e0.elapsed_time(e1), ws_n, dev)
+    evented_ms = max_over_ranks(
+        e0.elapsed_time(e1) if flush_buf is None else sum(e[0].elapsed_time(e[2]) for e in evs),
+        ws_n, dev)
     score_ms = [e[0].elapsed_time(e[1]) for e in evs]
     topk_ms = [e[1].elapsed_time(e[2]) for e in evs]
 
@@ -315,13 +372,19 @@ def run_ours(args):
 
     ab = algorithmic_bytes(batch)
     score_avg_ms = sum(score_ms) / len(score_ms)
+    wide = is_wide(s)
     achieved = ab["score"] / (score_avg_ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
+    tflops = ab["flops"] / (score_avg_ms * 1e-3) / 1e12
+    tpeak, tpeak_src = measured_tensor_peak(s.k_dtype)
+    # the bound is whichever ideal time is longer: bytes at the copy peak or
+    # useful flops at the tensor peak
+    tensor_bound = ab["flops"] / (tpeak * 1e12) > ab["score"] / (peak * 1e9)
     traffic = None
     try:
         with open(TRAFFIC_FILE) as fh:
             tr = json.load(fh).get(args.workload)
-        if tr and tr.get("kernel_sha") == kernel_sha():
+        if tr and tr.get("kernel_sha") == kernel_sha(wide):
             traffic = tr["dram_bytes_per_launch"]
     except Exception:
         pass
@@ -343,14 +406,25 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             **workload_config(s, R, args, ws_n),
-            "l2": f"inputs larger than L2 ({ab['keys'] / 1e6:.0f} MB of keys read per step), no flush",
+            "l2": (f"inputs larger than L2 ({ab['keys'] / 1e6:.0f} MB of keys read per step), no flush"
+                   if flush_buf is None else
+                   f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MB write outside the "
+                   f"step's events; {ab['keys'] / 1e6:.1f} MB of keys per step)"),
             "aggregate_GBps": round(ws_n * ab["score"] / (ms_per_step * 1e-3) / 1e9, 1),
         },
         "roofline": {
-            "bound": "hbm", "kernel": "score_kernel", "achieved": round(achieved, 1),
-            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "peak_source": peak_src, "traffic": traffic,
+            **({"bound": "tensor", "kernel": "wide_kernel", "achieved": round(tflops, 1),
+                "peak": tpeak, "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                "peak_source": tpeak_src, "traffic": traffic,
+                "hbm_GBps": round(achieved, 1), "hbm_frac": round(achieved / peak, 4)}
+               if tensor_bound else
+               {"bound": "hbm", "kernel": "wide_kernel" if wide else "score_kernel",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": traffic,
+                "tensor_TFLOPs": round(tflops, 1), "tensor_frac": round(tflops / tpeak, 4)}),
             "algorithmic_bytes_per_launch": ab["score"],
+            "algorithmic_flops_per_launch": ab["flops"],
+            "key_reads_per_request": ab["key_reads_per_request"],
             "score_us": round(score_avg_ms * 1e3, 3), "topk_us": round(sum(topk_ms) / len(topk_ms) * 1e3, 3),
             "frac_of_8TBps": round(achieved / 8000.0, 4),
             "timing": "value: K steps with no events between the kernels; score_us, topk_us "

@@ -16,8 +16,9 @@
 // blocks of the flattened (group, block) list):
 //   warp 0      TMA producer: the group's query tile (bf16 / e4m3) and each
 //               block's two key pages (+ their scales) into a ring of stages;
-//   warp 1      allocates 256 TMEM columns (two 128-column accumulators); lane 0
-//               issues the MMAs of a block and commits them to mbarriers;
+//   warp 1      allocates 512 TMEM columns (a ring of four 128-column fp32
+//               accumulators); lane 0 issues the MMAs of a block and commits
+//               them to mbarriers;
 //   warps 2..5  epilogue: thread = tile row; tcgen05.ld of its 128 scores, the
 //               row's mask and block score, one workspace write per row;
 //   warps 6..9  (NVFP4 keys) decode a block's e2m1 codes x E4M3 group scales into
@@ -41,7 +42,8 @@ namespace idx {
 namespace {
 
 constexpr int kWRows = 128;     // tile rows (MMA M)
-constexpr int kTmemCols = 256;  // two fp32 accumulators of 128 columns
+constexpr int kAcc = 4;          // fp32 accumulators of 128 columns in the TMEM ring
+constexpr int kTmemCols = 128 * kAcc;
 constexpr unsigned int kErrBadPage = 1u;  // IDX_DEVERR_BAD_PAGE
 constexpr unsigned int kErrTimeout = 2u;  // IDX_DEVERR_TIMEOUT
 constexpr unsigned int kErrLenClamped = 4u;  // IDX_DEVERR_LEN_CLAMPED
@@ -54,7 +56,7 @@ struct WCfg<kBf16> {
   static constexpr int kStageBytes = 32768; // 128 tokens x 256 B: two 16 KB K-halves
   static constexpr int kPagePayload = 16384;
   static constexpr int kPageScale = 0;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr int kDecStages = 0;
   static constexpr int kDecWarps = 0;
   static constexpr uint32_t kIdesc = instr_desc(1u, 128, 128);  // bf16 x bf16
@@ -65,7 +67,7 @@ struct WCfg<kFp8> {
   static constexpr int kStageBytes = 16384; // 128 tokens x 128 B
   static constexpr int kPagePayload = 8192;
   static constexpr int kPageScale = 256;    // 64 fp32
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 10;
   static constexpr int kDecStages = 0;
   static constexpr int kDecWarps = 0;
   static constexpr uint32_t kIdesc = instr_desc(0u, 128, 128);  // e4m3 x e4m3
@@ -76,7 +78,7 @@ struct WCfg<kNvfp4> {
   static constexpr int kStageBytes = 8192;  // raw codes of 128 tokens (64 B each)
   static constexpr int kPagePayload = 4096;
   static constexpr int kPageScale = 512;    // 64 x 8 E4M3 bytes
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 6;
   static constexpr int kDecStages = 3;      // decoded f16 tiles, 32 KB each
   static constexpr int kDecWarps = 4;
   static constexpr uint32_t kIdesc = instr_desc(0u, 128, 128);  // f16 x f16
@@ -92,8 +94,8 @@ struct WLayout {
   static constexpr int kDecOff = kStageOff + S * C::kStageBytes;
   static constexpr int kScaleOff = kDecOff + SD * 32768;
   static constexpr int kBarOff = kScaleOff + S * 2 * C::kPageScale;
-  // full[S] empty[S] dfull[SD] dempty[SD] afull[2] aempty[2] qfull qempty done
-  static constexpr int kNumBars = 2 * S + 2 * SD + 7;
+  // full[S] empty[S] dfull[SD] dempty[SD] afull[kAcc] aempty[kAcc] qfull qempty done
+  static constexpr int kNumBars = 2 * S + 2 * SD + 2 * kAcc + 3;
   static constexpr int kCtlOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kGroupOff = kCtlOff + 64;
   static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
@@ -114,11 +116,17 @@ struct WLayout {
     return sb + kBarOff + 8 * (2 * S + 2 * SD + j);
   }
   __device__ static uint32_t aempty(uint32_t sb, int j) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 + j);
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + kAcc + j);
   }
-  __device__ static uint32_t qfull(uint32_t sb) { return sb + kBarOff + 8 * (2 * S + 2 * SD + 4); }
-  __device__ static uint32_t qempty(uint32_t sb) { return sb + kBarOff + 8 * (2 * S + 2 * SD + 5); }
-  __device__ static uint32_t done(uint32_t sb) { return sb + kBarOff + 8 * (2 * S + 2 * SD + 6); }
+  __device__ static uint32_t qfull(uint32_t sb) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kAcc);
+  }
+  __device__ static uint32_t qempty(uint32_t sb) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kAcc + 1);
+  }
+  __device__ static uint32_t done(uint32_t sb) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kAcc + 2);
+  }
 };
 
 __device__ __forceinline__ float fmax_nf(float a, float b) { return a > b ? a : b; }
@@ -155,23 +163,27 @@ __device__ __forceinline__ void wlocate(const int* gpre, int V, int u, int& v, i
   b = u - gpre[lo];
 }
 
-// Page ids of block b of group v for lanes 0 and 1 (-1: no second page,
-// -2: bad page id, not read).
-__device__ __forceinline__ int wload_page(const ScoreArgs& a, const int* gpre, const int* gslot,
-                                          int v, int b, int lane, unsigned int* flags) {
-  int p = -1;
-  if (lane < 2) {
-    const int word = gslot[v];
-    const int slot = word & 0x7fffffff;
-    const bool last = b == gpre[v + 1] - gpre[v] - 1;
-    const bool want = lane == 0 || !(last && word < 0);
-    if (want) {
-      p = __ldg(a.page_table + (size_t)slot * a.max_pages + 2 * b + lane);
-      if (p < 0 || p >= a.num_pages) {
-        atomicOr(flags, kErrBadPage);
-        p = -2;
-      }
-    }
+// The unit after (v, b) in the flattened list (groups without blocks skipped).
+__device__ __forceinline__ void wnext(const int* gpre, int V, int& v, int& b) {
+  ++b;
+  while (v < V - 1 && b >= gpre[v + 1] - gpre[v]) {
+    ++v;
+    b = 0;
+  }
+}
+
+// Page `which` (0, 1) of block b of group v: -1 when the group's last block needs
+// only one page, -2 for a page id outside the pool (flagged, not read).
+__device__ __forceinline__ int wpage(const ScoreArgs& a, const int* gpre, const int* gslot, int v,
+                                     int b, int which, unsigned int* flags) {
+  const int word = gslot[v];
+  const int slot = word & 0x7fffffff;
+  const bool last = b == gpre[v + 1] - gpre[v] - 1;
+  if (which == 1 && last && word < 0) return -1;
+  const int p = __ldg(a.page_table + (size_t)slot * a.max_pages + 2 * b + which);
+  if (p < 0 || p >= a.num_pages) {
+    atomicOr(flags, kErrBadPage);
+    return -2;
   }
   return p;
 }
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       mbar_init(L::dfull(sb, d), C::kDecWarps);
       mbar_init(L::dempty(sb, d), 1);
     }
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kAcc; ++j) {
       mbar_init(L::afull(sb, j), 1);
       mbar_init(L::aempty(sb, j), 4);
     }
@@ -413,9 +425,23 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     // ======================= producer =======================
     int prev_v = -1, nq = 0, i = 0;
     bool ok = true;
+    int v = 0, b = 0, wpg = -1;
+    if (u0 < u1) wlocate(gpre, V, u0, v, b);
     for (int u = u0; u < u1 && ok; ++u, ++i) {
-      int v, b;
-      wlocate(gpre, V, u, v, b);
+      const int k = (u - u0) & 15;
+      if (k == 0) {
+        // page ids of the next 16 blocks in one round trip: lane l looks up
+        // page l & 1 of block u + l / 2
+        const int uu = u + (lane >> 1);
+        wpg = -1;
+        if (uu < u1) {
+          int pv, pb;
+          wlocate(gpre, V, uu, pv, pb);
+          wpg = wpage(a, gpre, gslot, pv, pb, lane & 1, cta_flags);
+        }
+      }
+      const int p0 = __shfl_sync(0xffffffffu, wpg, 2 * k);
+      const int p1 = __shfl_sync(0xffffffffu, wpg, 2 * k + 1);
       if (v != prev_v) {
         if (KF != kNvfp4 && lane == 0) {
           // the previous tile's MMAs must be done with the query tile
@@ -441,8 +467,6 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       if (lane == 0 && i >= S && !mbar_wait_bounded(L::empty(sb, s), ((i / S) - 1) & 1)) ok = false;
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
-      const int pg = wload_page(a, gpre, gslot, v, b, lane, cta_flags);
-      const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
       if (lane == 0) {
         uint32_t tx = 0;
         if (p0 >= 0) tx += C::kPagePayload + C::kPageScale;
@@ -466,6 +490,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
           }
         }
       }
+      wnext(gpre, V, v, b);
     }
     if (!ok) {
       if (lane == 0) {
@@ -499,8 +524,8 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
           if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1)) { ok = false; break; }
           opnd = sb + L::kStageOff + s * C::kStageBytes;
         }
-        const int j = i & 1;
-        if (i >= 2 && !mbar_wait_bounded(L::aempty(sb, j), ((i >> 1) - 1) & 1)) { ok = false; break; }
+        const int j = i % kAcc;
+        if (i >= kAcc && !mbar_wait_bounded(L::aempty(sb, j), ((i / kAcc) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(j * 128);
         if (KF == kFp8) {
@@ -519,8 +544,9 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         if constexpr (KF == kNvfp4) tc_commit(L::dempty(sb, i % SD));
         else tc_commit(L::empty(sb, s));
         tc_commit(L::afull(sb, j));
-        int vn = -1, bn = 0;
-        if (u + 1 < u1) wlocate(gpre, V, u + 1, vn, bn);
+        int vn = v, bn = b;
+        if (u + 1 < u1) wnext(gpre, V, vn, bn);
+        else vn = -1;
         if (vn != v) tc_commit(L::qempty(sb));  // last block of this tile
         v = vn;
         b = bn;
@@ -540,9 +566,9 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     int Lrow = 0, out_row = -1;
     float post = 1.f, qs = 0.f;
     bool ok = true;
-    for (int u = u0; u < u1; ++u, ++i) {
-      int v, b;
-      wlocate(gpre, V, u, v, b);
+    int v = 0, b = 0;
+    if (u0 < u1) wlocate(gpre, V, u0, v, b);
+    for (int u = u0; u < u1; ++u, ++i, wnext(gpre, V, v, b)) {
       if (v != prev_v) {
         const WGroup gi = wgroup_info(a, v);
         const bool live = ti < gi.nrows && gi.nbk > 0;
@@ -562,8 +588,8 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         ++nq;
         prev_v = v;
       }
-      const int j = i & 1;
-      if (!mbar_wait_bounded(L::afull(sb, j), (i >> 1) & 1)) ok = false;
+      const int j = i % kAcc;
+      if (!mbar_wait_bounded(L::afull(sb, j), (i / kAcc) & 1)) ok = false;
       // the key scales this warp reads were written by the copy engine: observe
       // their arrival itself (already complete, since the MMA waited for it)
       if (KF == kFp8 && ok && !mbar_wait_bounded(L::full(sb, i % S), (i / S) & 1)) ok = false;
@@ -574,19 +600,25 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       RowScore sc(post);
       const bool whole = tbase + kBlock <= Lrow;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t raw[32];
+      for (int h = 0; h < 2; ++h) {
+        // two 32-column loads in flight per wait
+        uint32_t raw[2][32];
         __syncwarp();
-        tc_ld_32cols(trow + (uint32_t)(j * 128 + c4 * 32), raw);
+        tc_ld_32cols(trow + (uint32_t)(j * 128 + h * 64), raw[0]);
+        tc_ld_32cols(trow + (uint32_t)(j * 128 + h * 64 + 32), raw[1]);
         tc_wait_ld();
-        float x[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          x[k] = __uint_as_float(raw[k]);
-          if (KF == kFp8) x[k] = (x[k] * qs) * ks[c4 * 32 + k];
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c0 = h * 64 + hh * 32;
+          float x[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            x[k] = __uint_as_float(raw[hh][k]);
+            if (KF == kFp8) x[k] = (x[k] * qs) * ks[c0 + k];
+          }
+          if (whole) sc.template add32<false>(x, tbase + c0, Lrow);
+          else sc.template add32<true>(x, tbase + c0, Lrow);
         }
-        if (whole) sc.template add32<false>(x, tbase + c4 * 32, Lrow);
-        else sc.template add32<true>(x, tbase + c4 * 32, Lrow);
       }
       tc_fence_before();
       __syncwarp();

@@ -260,6 +260,17 @@ WORKLOADS = {
                               explicit_lens=[_verify_rows(4, [32767, 32768, 32769, 32770])] * 4),
     "verify_fp8_4x32k": Spec("verify_fp8_4x32k", 1008, "fp8_e4m3", "fp8_e4m3", 4, 4, 4, 1, 4, 64,
                              explicit_lens=[_verify_rows(4, [32767, 32768, 32769, 32770])] * 4),
+    # more than 16 packed rows (the 128-row tensor-core tiles): 8 draft rows x 8 heads
+    "verify_bf16_16x32k_p8g8": Spec("verify_bf16_16x32k_p8g8", 1009, "bf16", "bf16", 16, 8, 8,
+                                    1, 4, 64, len_range=(30000, 32768)),
+    # prefill chunks: 512 query tokens x 4 heads per request, the chunk ending the
+    # request's ~32K context (row j of the chunk has length L - 511 + j)
+    "prefill_nvfp4_4x32k_c512": Spec("prefill_nvfp4_4x32k_c512", 1010, "nvfp4", "bf16", 4, 512, 4,
+                                     1, 4, 64, len_range=(32000, 32768)),
+    "prefill_bf16_4x32k_c512": Spec("prefill_bf16_4x32k_c512", 1011, "bf16", "bf16", 4, 512, 4,
+                                    1, 4, 64, len_range=(32000, 32768)),
+    "prefill_fp8_4x32k_c512": Spec("prefill_fp8_4x32k_c512", 1012, "fp8_e4m3", "fp8_e4m3", 4, 512,
+                                   4, 1, 4, 64, len_range=(32000, 32768)),
 }
 
 
