@@ -200,6 +200,14 @@ def max_over_ranks(x: float, ws: int, dev) -> float:
     return float(t.item())
 
 
+def flush_l2(buf: torch.Tensor) -> None:
+    """Evict L2 before a timed step: write a buffer twice the size of L2, then
+    read it back, so the dirty lines of the write are written back to HBM here
+    and not during the step that follows."""
+    buf.fill_(1)
+    buf.view(torch.int32).max()
+
+
 def metric_name(args) -> str:
     """The headline metric on the default workload with the block-max score;
     any other workload or block score is named in the metric itself."""
@@ -260,11 +268,12 @@ def run_ours(args):
     fn = score_fn(idx, args)
 
     def step(events=None):
+        # on whatever stream is current: the caller's, or a graph's capture stream
         if events is not None:
             idx.idx_set_kernel_events(*events)
         fn(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
            s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, topk,
-           out_ids, out_sc, wsp, stream)
+           out_ids, out_sc, wsp, torch.cuda.current_stream(dev))
 
     for _ in range(args.warmup):
         step()
@@ -273,16 +282,42 @@ def run_ours(args):
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} during warm-up")
 
-    # ---- timed region 1: K steps exactly as a caller runs them ----------------
-    # (no events between the score and top-k launches: an event there stops the
-    # top-k kernel's launch from overlapping the score kernel's tail)
+    # ---- CUDA graphs: a serving loop captures the step once and replays it, so
+    # the timed steps carry no per-call host cost.  A graph holds n_per steps
+    # (n_per divides K) and is replayed K / n_per times.
+    n_per = max(d for d in range(1, min(args.steps, 25) + 1) if args.steps % d == 0)
+    reps = args.steps // n_per
     # inputs that fit in L2 (129 MB) get it flushed before every step (a 256 MB
-    # write, outside each step's own pair of events); larger inputs stream
-    # through it anyway and run back to back
+    # write and read, outside the step's own pair of events); larger inputs
+    # stream through it anyway and run back to back
     in_bytes = (payload.numel() + (0 if scale is None else scale.numel()) +
                 q.numel() * q.element_size())
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) \
         if in_bytes < 2 * L2_BYTES else None
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain):
+        for _ in range(1 if flush_buf is not None else n_per):
+            step()
+    # per-kernel events recorded by the library inside the graph (external nodes)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_per)]
+    for trio in evs:            # torch creates an event's CUDA handle on its first record()
+        for e in trio:
+            e.record(stream)
+    g_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ev):
+        for k in range(n_per):
+            if flush_buf is not None:
+                flush_l2(flush_buf)
+            step(evs[k])
+    for _ in range(2):
+        g_plain.replay()
+        g_ev.replay()
+    torch.cuda.synchronize(dev)
+    flags = idx.idx_workspace_errors(wsp)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} in the graph replays")
+
+    # ---- timed region 1: K steps back to back (graph replays) ------------------
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
@@ -292,8 +327,8 @@ def run_ours(args):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for _ in range(args.steps):
-            step()
+        for _ in range(reps):
+            g_plain.replay()
         t1.record(stream)
         torch.cuda.synchronize(dev)
         run_ms = t0.elapsed_time(t1)
@@ -301,67 +336,77 @@ def run_ours(args):
         pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(args.steps)]
         for a_ev, b_ev in pairs:
-            flush_buf.fill_(1)
+            flush_l2(flush_buf)
             a_ev.record(stream)
-            step()
+            g_plain.replay()
             b_ev.record(stream)
         torch.cuda.synchronize(dev)
         run_ms = sum(a_ev.elapsed_time(b_ev) for a_ev, b_ev in pairs)
     barrier(ws_n)
     total_ms = max_over_ranks(run_ms, ws_n, dev)
 
-    # ---- timed region 2: the same K steps with CUDA events recorded by the
-    # library on the launching stream around each kernel (per-kernel durations)
-    # torch creates an event's CUDA handle on its first record(); record each once
-    # here so the library can re-record the same handles inside the timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for trio in evs:
-        for e in trio:
-            e.record(stream)
+    # ---- timed region 2: the same K steps with the library's events around each
+    # kernel (per-kernel durations on the launching stream)
     barrier(ws_n)
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        if flush_buf is not None:
-            flush_buf.fill_(1)
-        step(evs[k])
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    score_ms, topk_ms, step_ms = [], [], []
+    for _ in range(reps):
+        g_ev.replay()
+        torch.cuda.synchronize(dev)
+        score_ms += [e[0].elapsed_time(e[1]) for e in evs]
+        topk_ms += [e[1].elapsed_time(e[2]) for e in evs]
+        step_ms += [e[0].elapsed_time(e[2]) for e in evs]
     barrier(ws_n)
     clocks = sampler.stop()
-    evented_ms = max_over_ranks(
-        e0.elapsed_time(e1) if flush_buf is None else sum(e[0].elapsed_time(e[2]) for e in evs),
-        ws_n, dev)
-    score_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    topk_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    evented_ms = max_over_ranks(sum(step_ms), ws_n, dev)
 
     # ---- ablation: the same step with every draft row scored on its own -------
     ablation = None
     if not args.no_ablation:
         n_ab = max(10, min(args.steps, 100))
-        for _ in range(3):
+
+        def perrow(events=None):
+            if events is not None:
+                idx.idx_set_kernel_events(*events)
             idx.idx_score_topk_perrow(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
                                       s.packed_queries, s.gqa, s.init_blocks, s.local_blocks,
-                                      topk, out_ids, out_sc, wsp, stream)
-        abev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ab)]
-        for trio in abev:
-            for e in trio:
-                e.record(stream)
+                                      topk, out_ids, out_sc, wsp, torch.cuda.current_stream(dev))
+
+        for _ in range(3):
+            perrow()
+        abev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in abev:
+            e.record(stream)
+        g_ab = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ab):
+            perrow()
+        g_abev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_abev):
+            perrow(abev)
+        g_ab.replay()
         torch.cuda.synchronize(dev)
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for k in range(n_ab):
-            idx.idx_set_kernel_events(*abev[k])
-            idx.idx_score_topk_perrow(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
-                                      s.packed_queries, s.gqa, s.init_blocks, s.local_blocks,
-                                      topk, out_ids, out_sc, wsp, stream)
+        for _ in range(n_ab):
+            if flush_buf is not None:
+                flush_l2(flush_buf)
+            g_ab.replay()
         a1.record(stream)
         torch.cuda.synchronize(dev)
-        ab_us = a0.elapsed_time(a1) * 1e3 / n_ab
-        ab_score = sum(e[0].elapsed_time(e[1]) for e in abev) / n_ab * 1e3
+        ab_score = 0.0
+        ab_step = 0.0
+        for _ in range(n_ab):
+            if flush_buf is not None:
+                flush_l2(flush_buf)
+            g_abev.replay()
+            torch.cuda.synchronize(dev)
+            ab_score += abev[0].elapsed_time(abev[1])
+            ab_step += abev[0].elapsed_time(abev[2])
+        ab_score = ab_score / n_ab * 1e3
+        # with the L2 flush the back-to-back pass also holds the flushes: use the
+        # evented steps then
+        ab_us = (a0.elapsed_time(a1) * 1e3 / n_ab) if flush_buf is None else ab_step / n_ab * 1e3
         ablation = {"variant": "per-row (each draft row its own decode row, keys read P times)",
                     "us_per_step": round(ab_us, 3), "score_us": round(ab_score, 3),
                     "slowdown_vs_packed": round(ab_us / (total_ms / args.steps * 1e3), 3),
@@ -408,8 +453,8 @@ def run_ours(args):
             **workload_config(s, R, args, ws_n),
             "l2": (f"inputs larger than L2 ({ab['keys'] / 1e6:.0f} MB of keys read per step), no flush"
                    if flush_buf is None else
-                   f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MB write outside the "
-                   f"step's events; {ab['keys'] / 1e6:.1f} MB of keys per step)"),
+                   f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MB written then read, "
+                   f"outside the step's events; {ab['keys'] / 1e6:.1f} MB of keys per step)"),
             "aggregate_GBps": round(ws_n * ab["score"] / (ms_per_step * 1e-3) / 1e9, 1),
         },
         "roofline": {
@@ -427,9 +472,11 @@ def run_ours(args):
             "key_reads_per_request": ab["key_reads_per_request"],
             "score_us": round(score_avg_ms * 1e3, 3), "topk_us": round(sum(topk_ms) / len(topk_ms) * 1e3, 3),
             "frac_of_8TBps": round(achieved / 8000.0, 4),
-            "timing": "value: K steps with no events between the kernels; score_us, topk_us "
-                      "and achieved: CUDA events the library records around each kernel on "
-                      "the launching stream in a second pass of K steps",
+            "timing": "value: K steps replayed from CUDA graphs (n_per steps per graph), no "
+                      "events between the kernels; score_us, topk_us and achieved: CUDA "
+                      "events the library records around each kernel (external event "
+                      "nodes of a second graph) in a second pass of K steps",
+            "steps_per_graph": n_per,
             "step_us_with_kernel_events": round(evented_ms / args.steps * 1e3, 3),
         },
         "e2e": e2e,

@@ -37,6 +37,18 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Record a caller-supplied timing event on the stream; while the stream is being
+// captured into a CUDA graph the record becomes an external event node, so the
+// event still carries a timestamp each time the graph is replayed.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
 int64_t payload_row_bytes(int dtype) {
   switch (dtype) {
     case IDX_BF16: return 256;
@@ -71,11 +83,47 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// The last few tensor maps this host thread encoded, keyed by what they
+// describe, so a caller that reuses its pool and query buffers (a serving loop)
+// pays for the encoding once.
+struct MapCache {
+  struct Entry {
+    int kind, dtype;
+    const void* ptr;
+    int64_t rows;
+    CUtensorMap map;
+  };
+  static constexpr int kEntries = 8;
+  Entry e[kEntries];
+  int n = 0, next = 0;
+  const CUtensorMap* find(int kind, int dtype, const void* ptr, int64_t rows) const {
+    for (int i = 0; i < n; ++i)
+      if (e[i].kind == kind && e[i].dtype == dtype && e[i].ptr == ptr && e[i].rows == rows)
+        return &e[i].map;
+    return nullptr;
+  }
+  void put(int kind, int dtype, const void* ptr, int64_t rows, const CUtensorMap& m) {
+    Entry& x = e[next];
+    x.kind = kind;
+    x.dtype = dtype;
+    x.ptr = ptr;
+    x.rows = rows;
+    x.map = m;
+    next = (next + 1) % kEntries;
+    if (n < kEntries) ++n;
+  }
+};
+thread_local MapCache g_maps;
+
 // Tensor map over the payload plane, one 64-row (one page) box per load:
 //  bf16: 128 bf16 per row, box 64 x 64 (two boxes per page), 128-byte swizzle
 //  fp8:  128 bytes per row, box 128 x 64, 128-byte swizzle
 //  fp4:  64 bytes per row,  box 64 x 64,  64-byte swizzle
 int make_payload_map(int dtype, const void* payload, int64_t num_pages, CUtensorMap* map) {
+  if (const CUtensorMap* hit = g_maps.find(0, dtype, payload, num_pages)) {
+    *map = *hit;
+    return IDX_OK;
+  }
   auto fn = encode_fn();
   if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t rows = (cuuint64_t)num_pages * idx::kPage;
@@ -101,6 +149,7 @@ int make_payload_map(int dtype, const void* payload, int64_t num_pages, CUtensor
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  g_maps.put(0, dtype, payload, num_pages, *map);
   return IDX_OK;
 }
 
@@ -109,6 +158,10 @@ int make_payload_map(int dtype, const void* payload, int64_t num_pages, CUtensor
 // 128 rows high with the 128-byte swizzle the MMA operand descriptors expect.
 // Rows past the end read as zeros.
 int make_q_map(int q_dtype, const void* q, int64_t rows, CUtensorMap* map) {
+  if (const CUtensorMap* hit = g_maps.find(1, q_dtype, q, rows)) {
+    *map = *hit;
+    return IDX_OK;
+  }
   auto fn = encode_fn();
   if (!fn) return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {128, (cuuint64_t)rows};
@@ -130,6 +183,7 @@ int make_q_map(int q_dtype, const void* q, int64_t rows, CUtensorMap* map) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(IDX_ERR_CUDA, "cuTensorMapEncodeTiled (query rows) failed (%d)", (int)r);
+  g_maps.put(1, q_dtype, q, rows, *map);
   return IDX_OK;
 }
 
@@ -231,11 +285,11 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
   }
   cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
   g_ev[0] = g_ev[1] = g_ev[2] = nullptr;
-  if (ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
+  if (ev[0] && (e = record_event(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
   e = wide ? idx::launch_wide(k_dtype, block_score, sa, map, qmap, st)
            : idx::launch_score(k_dtype, block_score, sa, map, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
-  if (ev[1] && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
+  if (ev[1] && (e = record_event(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
 
   idx::TopkArgs ta;
   ta.blockmax = sa.blockmax;
@@ -257,7 +311,7 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
   ta.topk = topk;
   e = idx::launch_topk(ta, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the top-k kernel");
-  if (ev[2] && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
+  if (ev[2] && (e = record_event(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
   return IDX_OK;
 }
 

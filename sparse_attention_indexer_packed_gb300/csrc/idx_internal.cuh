@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace idx {
 
 constexpr int kPage = 64;     // tokens per page
@@ -65,6 +67,51 @@ struct TopkArgs {
   int R, P, G, M;
   int init_blocks, local_blocks, topk;
 };
+
+// ---- host-side launch helpers: keep a call's CPU cost to its launches -------
+// Streaming multiprocessors of device `dev`, looked up once per device.
+inline int cached_sm_count(int dev) {
+  static std::atomic<int> cache[64];
+  int n = 0;
+  if (dev >= 0 && dev < 64) n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (`done` is a
+// per-kernel bit mask of the devices already set).
+template <class Kernel>
+inline cudaError_t smem_limit_once(Kernel kernel, int bytes, int dev,
+                                   std::atomic<unsigned long long>& done) {
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Launch as a programmatic dependent of the previous kernel on the stream: the
+// grid may become resident while that kernel finishes (once all its CTAs have
+// signalled griddepcontrol.launch_dependents or exited) and must execute
+// griddepcontrol.wait before it touches memory the earlier work writes.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // Record an error message for idx_last_error() on this host thread; returns status.
 int record_error(int status, const char* message);

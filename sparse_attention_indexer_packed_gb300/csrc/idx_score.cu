@@ -554,6 +554,10 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     fence_barrier_init();
   }
   if (threadIdx.x == 0) prefetch_tensormap(&payload_map);
+  // launched as a programmatic dependent of whatever ran before on the stream:
+  // everything above touches only this CTA; from here on inputs are read and
+  // the workspace written, so wait for that work to complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- group table: block prefix sums and slots of every group -------------
   const int V = a.perrow ? a.R * a.P : a.R;
@@ -748,19 +752,19 @@ std::atomic<int> g_grid_limit{0};
 template <int KF, class Score>
 cudaError_t launch_kf(const ScoreArgs& a, const CUtensorMap& map, cudaStream_t stream) {
   using L = Layout<KF>;
+  static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(score_kernel<KF, Score>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kSmemBytes);
+  const int sms = cached_sm_count(dev);
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  e = smem_limit_once(score_kernel<KF, Score>, L::kSmemBytes, dev, attr_done);
   if (e != cudaSuccess) return e;
   const int lim = g_grid_limit.load(std::memory_order_relaxed);
   int grid = (lim > 0 && lim < sms) ? lim : sms;
   if (grid > kMaxScoreCtas) grid = kMaxScoreCtas;
-  score_kernel<KF, Score><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, map);
+  e = launch_pdl(score_kernel<KF, Score>, grid, L::kThreads, L::kSmemBytes, stream, a, map);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Shared));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // the next call's score kernel may become resident as soon as every row of
+  // this grid has started (it waits for this grid to finish before it reads)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int row = blockIdx.x;
   const int r = row / a.M;
   const int i = row - r * a.M;
@@ -265,8 +268,14 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   const int rows = a.R * a.M;
   if (rows == 0) return cudaSuccess;
   const size_t smem = sizeof(Shared) + (size_t)a.nb_cap * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // the limit is raised once per device to what the largest page table
+  // (65536 pages: 32768 blocks) can need; each launch asks for its own size
+  static std::atomic<unsigned long long> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = smem_limit_once(topk_kernel, (int)(sizeof(Shared) + 32768 * sizeof(uint32_t)), dev,
+                      attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)rows);

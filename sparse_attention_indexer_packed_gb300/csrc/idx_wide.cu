@@ -19,12 +19,14 @@
 //   warp 1      allocates 512 TMEM columns (a ring of four 128-column fp32
 //               accumulators); lane 0 issues the MMAs of a block and commits
 //               them to mbarriers;
-//   warps 2..5  epilogue: thread = tile row; tcgen05.ld of its 128 scores, the
-//               row's mask and block score, one workspace write per row;
-//   warps 6..9  (NVFP4 keys) decode a block's e2m1 codes x E4M3 group scales into
-//               an f16 operand tile (ROCm/ATOM #2745: the products are exact);
-//               the epilogue warps also convert the bf16 query tile to f16 with a
-//               per-row power-of-two scale, undone on the result.
+//   warps 2..9  epilogue, two groups of four warps taking alternate blocks:
+//               thread = tile row; tcgen05.ld of its 128 scores, the row's mask
+//               and block score, one workspace write per row;
+//   warps 10..13 (NVFP4 keys) decode a block's e2m1 codes x E4M3 group scales
+//               into an f16 operand tile (ROCm/ATOM #2745: the products are
+//               exact); the first epilogue group also converts the bf16 query
+//               tile to f16 with a per-row power-of-two scale, undone on the
+//               result.
 // Every wait is bounded; a timeout sets IDX_DEVERR_TIMEOUT and the CTA winds down
 // (copies in flight are waited for, TMEM is freed).
 #include <cuda_bf16.h>
@@ -100,7 +102,10 @@ struct WLayout {
   static constexpr int kGroupOff = kCtlOff + 64;
   static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
   static constexpr int kSmemBytes = kBytes + 1024;
-  static constexpr int kWarps = 6 + C::kDecWarps;
+  // producer, MMA issuer, two epilogue groups of four warps, decoders
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kDecWarp0 = 2 + kEpiWarps;
+  static constexpr int kWarps = kDecWarp0 + C::kDecWarps;
   static constexpr int kThreads = 32 * kWarps;
   static_assert(kStageOff % 1024 == 0 && kDecOff % 1024 == 0, "operand tiles 1024-aligned");
   static_assert(C::kStageBytes % 1024 == 0, "stages 1024-aligned");
@@ -130,27 +135,6 @@ struct WLayout {
 };
 
 __device__ __forceinline__ float fmax_nf(float a, float b) { return a > b ? a : b; }
-
-// Geometry of wide group v = (request r, tile tau).
-struct WGroup {
-  int r, row0, nrows, base_row, slot, extent, nbk;
-};
-
-__device__ WGroup wgroup_info(const ScoreArgs& a, int v) {
-  WGroup g;
-  g.r = v / a.tiles;
-  g.row0 = (v - g.r * a.tiles) * kWRows;
-  g.nrows = min(kWRows, a.M - g.row0);
-  g.base_row = g.r * a.M + g.row0;
-  g.slot = __ldg(a.slot_ids + g.r);
-  const bool pad = g.slot < 0 || g.slot >= a.n_slots;
-  int ext = 0;
-  const int j0 = g.row0 / a.G, j1 = (g.row0 + g.nrows - 1) / a.G;
-  for (int j = j0; j <= j1; ++j) ext = max(ext, __ldg(a.row_lens + g.r * a.P + j));
-  g.extent = min(ext, a.max_pages * kPage);
-  g.nbk = (pad || g.extent <= 0) ? 0 : (g.extent + kBlock - 1) / kBlock;
-  return g;
-}
 
 __device__ __forceinline__ void wlocate(const int* gpre, int V, int u, int& v, int& b) {
   int lo = 0, hi = V - 1;  // largest v with gpre[v] <= u
@@ -250,10 +234,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // f16 query tile for NVFP4 keys: row i of the tile (one thread) is rescaled by
-// 2^qexp so its largest magnitude lies in [2^14, 2^15) and stored as f16; every
-// element within 2^-24 of that maximum is exact.  Returns 2^-qexp.
+// 2^qexp so its largest magnitude lies in [2^14, 2^15) and stored as f16 (when
+// `write`); every element within 2^-24 of that maximum is exact.  Returns 2^-qexp.
 __device__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i, int base_row,
-                               int nrows) {
+                               int nrows, bool write) {
   const bool valid = i < nrows;
   const uint4* src = reinterpret_cast<const uint4*>(a.q + (size_t)(base_row + i) * 256);
   float amax = 0.f;
@@ -273,6 +257,7 @@ __device__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i, int ba
   if (amax > 0.f) qexp = 14 - (((__float_as_uint(amax) >> 23) & 0xff) - 127);
   qexp = max(-100, min(100, qexp));
   const float up = ldexpf(1.f, qexp);
+  if (!write) return ldexpf(1.f, -qexp);
 #pragma unroll 4
   for (int c = 0; c < 16; ++c) {
     uint32_t o[4] = {0u, 0u, 0u, 0u};
@@ -376,22 +361,49 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     tmem_relinquish();
   }
 
+  // launched as a programmatic dependent of whatever ran before on the stream:
+  // everything above touches only this CTA; from here on inputs are read and
+  // the workspace written, so wait for that work to complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // ---- group table: block prefix sums and slots of every (request, tile) ----
+  // (1) every thread takes draft rows: a tile's extent is the longest of the
+  // draft rows any of its rows belongs to (one load per draft row, all in flight
+  // at once); (2) warp 0 turns extents into block counts and prefix sums.
   const int V = a.R * a.tiles;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) gpre[v] = 0;
+  if (threadIdx.x == 0) *cta_flags = 0u;
+  __syncthreads();
+  {
+    bool clamped = false;
+    const int RP = a.R * a.P;
+    const int cap = a.max_pages * kPage;
+    for (int x = threadIdx.x; x < RP; x += blockDim.x) {
+      const int L = __ldg(a.row_lens + x);
+      if (L <= 0) continue;
+      const int r = x / a.P, j = x - r * a.P;
+      const int t0 = (j * a.G) / kWRows, t1 = (j * a.G + a.G - 1) / kWRows;
+      for (int t = t0; t <= t1; ++t) atomicMax(&gpre[r * a.tiles + t], min(L, cap));
+      if (blockIdx.x == 0 && L > cap) {
+        const int slot = __ldg(a.slot_ids + r);
+        clamped |= slot >= 0 && slot < a.n_slots;
+      }
+    }
+    if (clamped) atomicOr(cta_flags, kErrLenClamped);
+  }
+  __syncthreads();
   if (warp == 0) {
     int run = 0;
-    bool clamped = false;
     for (int v0 = 0; v0 < V; v0 += 32) {
       const int v = v0 + lane;
       int nbk = 0, word = 0;
       if (v < V) {
-        const WGroup gi = wgroup_info(a, v);
-        nbk = gi.nbk;
-        const int rem = gi.extent - (nbk - 1) * kBlock;
-        word = (nbk > 0 ? gi.slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
-        if (blockIdx.x == 0 && gi.row0 == 0 && gi.slot >= 0 && gi.slot < a.n_slots)
-          for (int j = 0; j < a.P; ++j)
-            clamped |= __ldg(a.row_lens + gi.r * a.P + j) > a.max_pages * kPage;
+        const int ext = gpre[v];
+        const int slot = __ldg(a.slot_ids + v / a.tiles);
+        const bool pad = slot < 0 || slot >= a.n_slots;
+        nbk = (pad || ext <= 0) ? 0 : (ext + kBlock - 1) / kBlock;
+        const int rem = ext - (nbk - 1) * kBlock;  // tokens in the last block
+        word = (nbk > 0 ? slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
       }
       int incl = nbk;
 #pragma unroll
@@ -399,17 +411,16 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
+      __syncwarp();  // every lane has read its extent before any prefix is written
       if (v < V) {
         gpre[v] = run + incl - nbk;
         gslot[v] = word;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    clamped = __any_sync(0xffffffffu, clamped);
     if (lane == 0) {
       gpre[V] = run;
       ctl[0] = run;
-      *cta_flags = clamped ? kErrLenClamped : 0u;
     }
   }
   tc_fence_before();
@@ -557,8 +568,11 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       (void)mbar_wait_bounded(L::done(sb), 0, 200000000ull);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < L::kDecWarp0) {
     // ======================= epilogue =======================
+    // group eg takes the blocks with i % 2 == eg (accumulators eg, eg + 2); both
+    // groups walk every block to follow the tiles
+    const int eg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int ti = quarter * 32 + lane;  // tile row of this thread
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -570,24 +584,29 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     if (u0 < u1) wlocate(gpre, V, u0, v, b);
     for (int u = u0; u < u1; ++u, ++i, wnext(gpre, V, v, b)) {
       if (v != prev_v) {
-        const WGroup gi = wgroup_info(a, v);
-        const bool live = ti < gi.nrows && gi.nbk > 0;
-        out_row = live ? gi.base_row + ti : -1;
-        Lrow = live ? min(__ldg(a.row_lens + gi.r * a.P + (gi.row0 + ti) / a.G),
-                          a.max_pages * kPage)
-                    : 0;
+        const int r = v / a.tiles;
+        const int row0 = (v - r * a.tiles) * kWRows;
+        const int nrows = min(kWRows, a.M - row0);
+        const bool live = ti < nrows && gpre[v + 1] > gpre[v];
+        out_row = live ? r * a.M + row0 + ti : -1;
+        Lrow = live ? min(__ldg(a.row_lens + r * a.P + (row0 + ti) / a.G), a.max_pages * kPage) : 0;
         if (KF == kFp8) qs = live ? __ldg(a.q_scale + out_row) : 0.f;
         if (KF == kNvfp4) {
-          // every MMA of the previous tile has completed (its last block's
-          // accumulator was waited for below), so the query tile is free
-          post = convert_q_row(a, qtile, ti, gi.base_row, gi.nrows);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(L::qfull(sb));
+          // group 0 writes the f16 query tile once every MMA of the previous
+          // tile has completed; group 1 only derives its rows' scales
+          if (eg == 0 && nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
+          if (!__all_sync(0xffffffffu, ok)) break;
+          post = convert_q_row(a, qtile, ti, r * a.M + row0, nrows, eg == 0);
+          if (eg == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(L::qfull(sb));
+          }
         }
         ++nq;
         prev_v = v;
       }
+      if ((i & 1) != eg) continue;
       const int j = i % kAcc;
       if (!mbar_wait_bounded(L::afull(sb, j), (i / kAcc) & 1)) ok = false;
       // the key scales this warp reads were written by the copy engine: observe
@@ -631,7 +650,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     if (!ok && lane == 0) atomicOr(cta_flags, kErrTimeout);
   } else if constexpr (KF == kNvfp4) {
     // ======================= NVFP4 decoders =======================
-    const int n = (warp - 6) * 32 + lane;  // token of the block
+    const int n = (warp - L::kDecWarp0) * 32 + lane;  // token of the block
     bool ok = true;
     int i = 0;
     for (int u = u0; u < u1; ++u, ++i) {
@@ -667,19 +686,20 @@ template <int KF, class RowScore>
 cudaError_t launch_wide_kf(const ScoreArgs& a, const CUtensorMap& kmap, const CUtensorMap& qmap,
                            cudaStream_t stream) {
   using L = WLayout<KF>;
+  static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(wide_kernel<KF, RowScore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           L::kSmemBytes);
+  const int sms = cached_sm_count(dev);
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  e = smem_limit_once(wide_kernel<KF, RowScore>, L::kSmemBytes, dev, attr_done);
   if (e != cudaSuccess) return e;
   const int lim = grid_limit();
   int grid = (lim > 0 && lim < sms) ? lim : sms;
   if (grid > kMaxScoreCtas) grid = kMaxScoreCtas;
-  wide_kernel<KF, RowScore><<<grid, L::kThreads, L::kSmemBytes, stream>>>(a, kmap, qmap);
+  e = launch_pdl(wide_kernel<KF, RowScore>, grid, L::kThreads, L::kSmemBytes, stream, a, kmap,
+                 qmap);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
