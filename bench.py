@@ -485,7 +485,8 @@ def run_ours(args):
         "clocks": clocks,
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(batch, args) if ws_n == 1 else None
+        line["cpu_baseline"] = (cpu_baseline(batch, args)
+                                if ws_n == 1 and not args.no_cpu_baseline else None)
         print(json.dumps(line), flush=True)
     if ws_n > 1:
         import torch.distributed as dist
@@ -643,6 +644,8 @@ def main():
     ap.add_argument("--block-score", default="max", choices=["max", "lse"],
                     help="block score the selection ranks by (max: the headline step)")
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-row ablation timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle's CPU timing (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

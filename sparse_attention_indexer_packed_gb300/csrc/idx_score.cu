@@ -134,7 +134,9 @@ __device__ __forceinline__ int tile_row_len(const ScoreArgs& a, int v, int r, in
   return clamp_len(L, a.max_pages * kPage);
 }
 
-__device__ __forceinline__ float fmax_nan_free(float a, float b) { return a > b ? a : b; }
+// Scores are finite, so the max needs no NaN rule of its own: fmaxf is a single
+// FMNMX instruction (a compare-and-select pair would cost two).
+__device__ __forceinline__ float fmax_finite(float a, float b) { return fmaxf(a, b); }
 
 // Per-lane running block scores of the two tile rows a lane holds (row g and
 // g + 8).  add() folds the four accumulator values of one 8-token slice: v0, v1
@@ -151,20 +153,20 @@ struct MaxScore {
   __device__ __forceinline__ void add(float v0, float v1, float v2, float v3, int t0, int L0,
                                       int L1) {
     if (kMask) {
-      if (t0 < L0) m0 = fmax_nan_free(m0, v0);
-      if (t0 + 1 < L0) m0 = fmax_nan_free(m0, v1);
-      if (t0 < L1) m1 = fmax_nan_free(m1, v2);
-      if (t0 + 1 < L1) m1 = fmax_nan_free(m1, v3);
+      if (t0 < L0) m0 = fmax_finite(m0, v0);
+      if (t0 + 1 < L0) m0 = fmax_finite(m0, v1);
+      if (t0 < L1) m1 = fmax_finite(m1, v2);
+      if (t0 + 1 < L1) m1 = fmax_finite(m1, v3);
     } else {
-      m0 = fmax_nan_free(m0, fmax_nan_free(v0, v1));
-      m1 = fmax_nan_free(m1, fmax_nan_free(v2, v3));
+      m0 = fmax_finite(m0, fmax_finite(v0, v1));
+      m1 = fmax_finite(m1, fmax_finite(v2, v3));
     }
   }
   __device__ __forceinline__ void reduce() {
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
-      m0 = fmax_nan_free(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-      m1 = fmax_nan_free(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      m0 = fmax_finite(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmax_finite(m1, __shfl_xor_sync(0xffffffffu, m1, o));
     }
   }
   // a positive power of two commutes with the max: applied once, to the result
@@ -184,7 +186,7 @@ struct LseScore {
   __device__ __forceinline__ explicit LseScore(float post_scale)
       : c(post_scale * 1.4426950408889634f) {}
   __device__ __forceinline__ void push2(float& m, float& s, float x, float y) const {
-    const float mn = fmax_nan_free(m, fmax_nan_free(x, y));
+    const float mn = fmax_finite(m, fmax_finite(x, y));
     const float r = mn == -INFINITY ? 0.f : mn * c;  // all -inf so far: keep s = 0
     s = fmaf(s, ex2_approx(fmaf(m, c, -r)), ex2_approx(fmaf(x, c, -r)) + ex2_approx(fmaf(y, c, -r)));
     m = mn;
@@ -192,7 +194,7 @@ struct LseScore {
   __device__ __forceinline__ void merge(float& m, float& s, int o) const {
     const float om = __shfl_xor_sync(0xffffffffu, m, o);
     const float os = __shfl_xor_sync(0xffffffffu, s, o);
-    const float mn = fmax_nan_free(m, om);
+    const float mn = fmax_finite(m, om);
     const float r = mn == -INFINITY ? 0.f : mn * c;
     s = fmaf(s, ex2_approx(fmaf(m, c, -r)), os * ex2_approx(fmaf(om, c, -r)));
     m = mn;

@@ -134,7 +134,9 @@ struct WLayout {
   }
 };
 
-__device__ __forceinline__ float fmax_nf(float a, float b) { return a > b ? a : b; }
+// Scores are finite, so the max needs no NaN rule of its own: fmaxf is a single
+// FMNMX instruction (a compare-and-select pair would cost two).
+__device__ __forceinline__ float fmax_finite(float a, float b) { return fmaxf(a, b); }
 
 __device__ __forceinline__ void wlocate(const int* gpre, int V, int u, int& v, int& b) {
   int lo = 0, hi = V - 1;  // largest v with gpre[v] <= u
@@ -182,10 +184,10 @@ struct RowMax {
     float p = -INFINITY, q = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 32; k += 2) {
-      if (!kMask || t0 + k < L) p = fmax_nf(p, x[k]);
-      if (!kMask || t0 + k + 1 < L) q = fmax_nf(q, x[k + 1]);
+      if (!kMask || t0 + k < L) p = fmax_finite(p, x[k]);
+      if (!kMask || t0 + k + 1 < L) q = fmax_finite(q, x[k + 1]);
     }
-    m = fmax_nf(m, fmax_nf(p, q));
+    m = fmax_finite(m, fmax_finite(p, q));
   }
   __device__ __forceinline__ float out() const { return m * post; }
 };
@@ -202,8 +204,8 @@ struct RowLse {
     float mx = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 32; ++k)
-      if (!kMask || t0 + k < L) mx = fmax_nf(mx, x[k]);
-    const float mn = fmax_nf(m, mx);
+      if (!kMask || t0 + k < L) mx = fmax_finite(mx, x[k]);
+    const float mn = fmax_finite(m, mx);
     const float r = mn == -INFINITY ? 0.f : mn * c;
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
