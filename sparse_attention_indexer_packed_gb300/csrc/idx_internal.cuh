@@ -81,14 +81,22 @@ inline int cached_sm_count(int dev) {
   return n;
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device (`done` is a
-// per-kernel bit mask of the devices already set).
+// Once per device (`done` is a per-kernel bit mask of the devices already set):
+// raise a kernel's dynamic shared-memory limit to `bytes` (when > 0) and ask for
+// the largest shared-memory carveout.  Every kernel of the step prefers the same
+// carveout, so a programmatic dependent can become resident on an SM beside the
+// grid it follows instead of waiting for that SM to be reconfigured.
 template <class Kernel>
 inline cudaError_t smem_limit_once(Kernel kernel, int bytes, int dev,
                                    std::atomic<unsigned long long>& done) {
   const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaSuccess;
+  if (bytes > 0)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }

@@ -262,11 +262,216 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Rows of at most 32 * R blocks (short contexts, many rows: prefill chunks, wide
+// verify): one warp per row, four rows per CTA, no block-wide barrier.  The
+// row's candidate keys live in registers (element e = lane + 32 r is block
+// fi + e); radix passes of up to 8 bits over a warp-private 256-bin histogram,
+// starting below the bits every candidate shares, narrow to the threshold's
+// bin: when that bin is taken whole they stop; otherwise they end at the exact
+// c-th largest key T, keys above T are taken, and of the keys equal to T the
+// lowest ids, counted with ballots in id order.  The chosen entries are
+// compacted in id order and each is placed by its rank (key desc, id asc).
+// Same selection, outputs and score recovery as topk_kernel.
+// ---------------------------------------------------------------------------
+// Four rows per CTA and one 2 KB slot per warp (histogram while the threshold
+// is found, then the chosen list): 8 KB, small enough to sit beside a score CTA
+// on the same SM, so the programmatic launch still overlaps the score's tail.
+constexpr int kRowsPerCta = 4;
+
+union WarpSlot {
+  uint32_t hist[256];
+  unsigned long long list[256];
+};
+
+template <int R>
+__global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkArgs a) {
+  __shared__ WarpSlot sh[kRowsPerCta];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row = blockIdx.x * kRowsPerCta + warp;
+  if (row >= a.R * a.M) return;
+  uint32_t* hist = sh[warp].hist;
+  unsigned long long* list = sh[warp].list;
+  const int r = row / a.M;
+  const int i = row - r * a.M;
+  int32_t* out_ids = a.out_ids + (size_t)row * a.topk;
+  float* out_sc = a.out_scores + (size_t)row * a.topk;
+  const float* bm = a.blockmax + (size_t)row * a.nb_cap;
+
+  const int slot = __ldg(a.slot_ids + r);
+  int L = 0;
+  if (slot >= 0 && slot < a.n_slots) L = min(__ldg(a.row_lens + r * a.P + i / a.G), a.max_pages * kPage);
+  const int nb = L > 0 ? (L + kBlock - 1) / kBlock : 0;
+  const int fi = min(a.init_blocks, nb);       // forced init: [0, fi)
+  const int ls = max(fi, nb - a.local_blocks);  // forced local: [ls, nb)
+  const int nf = fi + (nb - ls);
+  const int ncand = ls - fi;                    // candidates: [fi, ls)
+  const int c = min(a.topk, nb) - nf;           // candidates to choose
+
+  for (int t = nf + max(c, 0) + lane; t < a.topk; t += 32) {
+    out_ids[t] = -1;
+    out_sc[t] = -INFINITY;
+  }
+  // the block scores are written by the score kernel this grid depends on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (row == 0 && lane == 0) {
+    *reinterpret_cast<volatile uint32_t*>(a.sched_counter) = 0u;
+    *reinterpret_cast<volatile unsigned long long*>(a.sched_tag) = kSchedTag;
+  }
+  for (int t = lane; t < nf; t += 32) {
+    const int id = t < fi ? t : ls + (t - fi);
+    out_ids[t] = id;
+    out_sc[t] = bm[id];
+  }
+  if (c <= 0) return;
+
+  uint32_t key[R];
+  bool act[R];
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const int e = lane + 32 * q;
+    act[q] = e < ncand;
+    key[q] = act[q] ? order_key(bm[fi + e]) : 0u;
+  }
+  bool sel[R];
+#pragma unroll
+  for (int q = 0; q < R; ++q) sel[q] = act[q];
+  if (ncand > c) {
+    // ---- threshold: radix passes of up to 8 bits, starting below the bits
+    // all candidates share, until the threshold's bin is taken whole or the
+    // exact c-th largest key T is known --------------------------------------
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+      if (act[q]) {
+        kmin = min(kmin, key[q]);
+        kmax = max(kmax, key[q]);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    int hi = 32 - __clz(kmin ^ kmax);  // bits [hi, 32) are common to all candidates
+    uint32_t pmask = hi >= 32 ? 0u : (0xffffffffu << hi);
+    uint32_t prefix = kmax & pmask, need = (uint32_t)c;
+    bool whole_bin = false;
+#pragma unroll 1
+    while (hi > 0) {
+      const int lo = max(hi - 8, 0);
+      const uint32_t dmask = (1u << (hi - lo)) - 1u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) hist[lane * 8 + k] = 0u;
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+        if (act[q] && (key[q] & pmask) == prefix) atomicAdd(&hist[(key[q] >> lo) & dmask], 1u);
+      __syncwarp();
+      // lane l owns bins 255 - 8 l - e, e = 0..7 (highest digits first)
+      uint32_t loc[8];
+      uint32_t sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        loc[e] = hist[255 - 8 * lane - e];
+        sum += loc[e];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - sum;
+      const bool mine = excl < need && need <= incl;
+      uint32_t digit = 0, left = 0, inbin = 0;
+      if (mine) {
+        uint32_t above = excl;
+        bool found = false;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (!found && above + loc[e] >= need) {
+            digit = (uint32_t)(255 - 8 * lane - e);
+            left = need - above;
+            inbin = loc[e];
+            found = true;
+          }
+          above += loc[e];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      need = __shfl_sync(0xffffffffu, left, src);
+      inbin = __shfl_sync(0xffffffffu, inbin, src);
+      prefix |= digit << lo;
+      pmask |= dmask << lo;
+      hi = lo;
+      __syncwarp();  // every lane has read the histogram before it is reused
+      if (need == inbin) {  // the whole threshold bin is chosen
+        whole_bin = true;
+        break;
+      }
+    }
+    if (whole_bin) {
+#pragma unroll
+      for (int q = 0; q < R; ++q) sel[q] = act[q] && (key[q] & pmask) >= prefix;
+    } else {
+      // T = prefix exactly: keys above it, then the `need` lowest ids equal to it
+      uint32_t base = 0;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const bool eq = act[q] && key[q] == prefix;
+        const unsigned m = __ballot_sync(0xffffffffu, eq);
+        const uint32_t rk = base + __popc(m & ((1u << lane) - 1u));
+        sel[q] = act[q] && (key[q] > prefix || (eq && rk < need));
+        base += __popc(m);
+      }
+    }
+  }
+  // ---- compact the chosen entries in id order, then place each by rank -----
+  int n = 0;
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const unsigned m = __ballot_sync(0xffffffffu, sel[q]);
+    if (sel[q]) list[n + __popc(m & ((1u << lane) - 1u))] = pack(key[q], fi + lane + 32 * q);
+    n += __popc(m);
+  }
+  __syncwarp();
+  for (int j = lane; j < n; j += 32) {
+    const unsigned long long x = list[j];
+    int rank = 0;
+#pragma unroll 8
+    for (int k = 0; k < n; ++k) rank += list[k] > x ? 1 : 0;
+    out_ids[nf + rank] = 0x7fffffff - (int)(uint32_t)(x & 0xffffffffull);
+    out_sc[nf + rank] = key_value((uint32_t)(x >> 32));
+  }
+}
+
+template <int R>
+cudaError_t launch_topk_warp(const TopkArgs& a, int rows, cudaStream_t stream) {
+  static std::atomic<unsigned long long> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = smem_limit_once(topk_warp_kernel<R>, 0, dev, attr_done);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(topk_warp_kernel<R>, (rows + kRowsPerCta - 1) / kRowsPerCta,
+                    32 * kRowsPerCta, 0, stream, a);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   const int rows = a.R * a.M;
   if (rows == 0) return cudaSuccess;
+  // many short rows: a warp per row (measured: below about 16 rows per SM the
+  // CTA-per-row kernel's shorter per-row latency wins)
+  int cur = 0;
+  if (cudaGetDevice(&cur) == cudaSuccess && rows >= 16 * cached_sm_count(cur)) {
+    if (a.nb_cap <= 64) return launch_topk_warp<2>(a, rows, stream);
+    if (a.nb_cap <= 128) return launch_topk_warp<4>(a, rows, stream);
+    if (a.nb_cap <= 256) return launch_topk_warp<8>(a, rows, stream);
+  }
   const size_t smem = sizeof(Shared) + (size_t)a.nb_cap * sizeof(uint32_t);
   // the limit is raised once per device to what the largest page table
   // (65536 pages: 32768 blocks) can need; each launch asks for its own size

@@ -311,3 +311,25 @@ def test_batch_invariance_of_a_request():
     o = _gpu.run(b2, planes=planes)
     assert np.array_equal(a.ids[0], o.ids[0])
     assert np.array_equal(a.scores[0].view(np.uint32), o.scores[0].view(np.uint32))
+
+
+def test_topk_warp_rows_match_cta_rows():
+    """Many rows of at most 256 blocks (here 4 prefill-like requests of 256
+    query tokens x 4 heads: 4096 rows) take the warp-per-row top-k; the same
+    rows behind a page table wider than 512 pages take the CTA-per-row one.
+    Both must give the oracle's selection and agree bit for bit, including rows
+    whose scores are all equal (zero queries: every tie goes to the lower id)."""
+    spec = workloads.small_spec("tk", 501, "bf16", "bf16", R=4, P=256, G=4,
+                                len_range=(300, 9000), topk=16)
+    b = workloads.make_batch(spec)
+    b.q[1] = 0                      # request 1: every block score 0
+    b.q[2, 7, 1] = 0                # one row of request 2
+    planes = _gpu.device_planes(b)
+    warp = _gpu.run(b, planes=planes)
+    wide_pt = torch.cat([b.page_table, b.page_table[:, :1].repeat(1, 600)], dim=1)
+    cta = _gpu.run(b, planes=planes, page_table=wide_pt)
+    assert warp.flags == 0 and cta.flags == 0
+    assert np.array_equal(warp.ids, cta.ids)
+    assert np.array_equal(warp.scores.view(np.uint32), cta.scores.view(np.uint32))
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_all_rows(b, warp, ref)
