@@ -11,10 +11,11 @@ the method, each citing the page passage it follows:
 
 * ``formats``  - E4M3 / E2M1 decoding, round-to-nearest-even encoders, the
   NVFP4 per-16 quantiser (ROCm/ATOM #2745, Summary) and dequantisation.
-* ``index``    - per-row causal-masked q.k scores, per-128-token block max,
-  forced init/local blocks and block top-k (sglang #45451, Modifications;
-  sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring for EAGLE verify
-  rows", Modifications 1 and Accuracy Tests).
+* ``index``    - per-row causal-masked q.k scores, per-128-token block max
+  (or log-sum-exp), forced init/local blocks and block top-k (sglang #45451,
+  Modifications; sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring for
+  EAGLE verify rows", Modifications 1 and Accuracy Tests), and the per-shard
+  selection and merge of indexer context parallelism.
 
 Pins (tests under ``-m "not gpu"``) tie it to facts outside itself: torch's own
 float8_e4m3fn conversion, hand-worked NVFP4 groups, exhaustive bf16

@@ -122,6 +122,61 @@ def select_row(blockmax: np.ndarray, init_blocks: int, local_blocks: int, topk: 
     return ids, scores
 
 
+def shard_select(blockmax: np.ndarray, b0: int, b1: int, init_blocks: int, local_blocks: int,
+                 topk: int):
+    """What one context shard of a row contributes (indexer context parallelism:
+    sglang #42614 names the per-shard scorer score_local_blocks; reading: rank w
+    holds the row's blocks [b0, b1) and scores only those).  ``blockmax`` is the
+    row's whole block-score vector; only [b0, b1) of it is used.  The forced set
+    and the number c of candidates to choose come from the row's global block
+    count.  The shard emits its forced blocks (ascending), then its best
+    min(c, its candidates) candidates by (score desc, id asc), then (-1, -inf)
+    pads.  Returns (ids int64 [topk], scores float64 [topk])."""
+    nb = len(blockmax)
+    forced = forced_blocks(nb, init_blocks, local_blocks)
+    fset = set(forced)
+    c = max(0, min(topk, nb) - len(forced))
+    lo, hi = max(0, b0), min(nb, b1)
+    mine_f = [b for b in forced if lo <= b < hi]
+    cands = [b for b in range(lo, hi) if b not in fset]
+    cands.sort(key=lambda b: (-blockmax[b], b))
+    chosen = mine_f + cands[:c]
+    ids = np.full(topk, -1, dtype=np.int64)
+    scores = np.full(topk, -np.inf, dtype=np.float64)
+    ids[:len(chosen)] = chosen
+    scores[:len(chosen)] = [blockmax[b] for b in chosen]
+    return ids, scores
+
+
+def merge_shards(lists, nb: int, init_blocks: int, local_blocks: int, topk: int):
+    """Re-select a row from its shards' lists (the exchange step of indexer
+    context parallelism): the forced blocks of the row's global block count,
+    ascending, with the scores their shard reported, then the best c of all the
+    shards' other entries by (score desc, id asc), then pads.  ``lists`` is a
+    sequence of (ids, scores) as shard_select returns them."""
+    forced = forced_blocks(nb, init_blocks, local_blocks)
+    fset = set(forced)
+    c = max(0, min(topk, nb) - len(forced))
+    fscore = {}
+    pool = []
+    for ids, scores in lists:
+        for b, v in zip(ids, scores):
+            b = int(b)
+            if b < 0:
+                continue
+            if b in fset:
+                fscore[b] = v
+            else:
+                pool.append((b, v))
+    pool.sort(key=lambda e: (-e[1], e[0]))
+    chosen = [(b, fscore[b]) for b in forced] + pool[:c]
+    ids = np.full(topk, -1, dtype=np.int64)
+    scores = np.full(topk, -np.inf, dtype=np.float64)
+    ids[:len(chosen)] = [b for b, _ in chosen]
+    scores[:len(chosen)] = [v for _, v in chosen]
+    return ids, scores
+
+
 def request_slot(slot_ids, r: int) -> int:
     """The slot a request's keys live under (never its row or group index)."""
     return int(slot_ids[r])

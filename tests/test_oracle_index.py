@@ -369,3 +369,51 @@ def test_blocklse_closed_forms_and_bounds():
     for b in range(3):
         m, v = mx.blockmax[(0, 1)][b], lse.blockmax[(0, 1)][b]
         assert m <= v <= m + math.log(counts[b]) + 1e-12
+
+
+# ---- indexer context parallelism: shard lists and their merge --------------
+def _random_partition(rng, nb):
+    cuts = sorted(set(rng.integers(0, nb + 1, size=rng.integers(0, 4)).tolist()) | {0, nb})
+    return list(zip(cuts[:-1], cuts[1:]))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_merge_of_shards_equals_the_single_device_selection(seed):
+    """For any split of a row's blocks into contiguous shards, merging the
+    shards' lists gives exactly select_row over the whole row: each shard keeps
+    its best c candidates, so every globally chosen block reaches the merge.
+    Rows with many tied scores (few distinct values) are included."""
+    rng = np.random.default_rng(seed)
+    nb = int(rng.integers(1, 60))
+    if seed % 3 == 0:
+        bm = rng.integers(0, 3, size=nb).astype(np.float64)   # heavy ties
+    else:
+        bm = rng.standard_normal(nb)
+    init, local = int(rng.integers(0, 3)), int(rng.integers(0, 4))
+    topk = int(rng.integers(init + local, init + local + 12)) or 1
+    parts = _random_partition(rng, nb)
+    lists = [index.shard_select(bm, b0, b1, init, local, topk) for b0, b1 in parts]
+    ids, sc = index.merge_shards(lists, nb, init, local, topk)
+    ref_ids, ref_sc = index.select_row(bm, init, local, topk)
+    assert ids.tolist() == ref_ids.tolist()
+    assert sc.tolist() == ref_sc.tolist()
+
+
+def test_shard_lists_brute_force():
+    """A shard's list on a tiny row, against brute force over every subset of
+    its candidates: the chosen ones are the subset of the right size whose
+    sorted (score desc, id asc) sequence is lexicographically best."""
+    bm = np.array([0.5, 2.0, -1.0, 2.0, 0.25, 3.0, 0.5, 1.0])
+    init, local, topk = 1, 1, 5          # forced {0, 7}; c = 3
+    ids, sc = index.shard_select(bm, 2, 7, init, local, topk)
+    cands = [2, 3, 4, 5, 6]
+    best = None
+    for sub in itertools.combinations(cands, 3):
+        key = sorted(((-bm[b], b) for b in sub))
+        if best is None or key < best[0]:
+            best = (key, sub)
+    want = [b for _, b in best[0]]
+    assert ids.tolist() == want + [-1, -1]
+    # a shard holding a forced block lists it first
+    ids0, _ = index.shard_select(bm, 0, 3, init, local, topk)
+    assert ids0.tolist()[:1] == [0] and set(ids0.tolist()[1:3]) == {1, 2}
