@@ -41,6 +41,7 @@ extern "C" {
 #define IDX_MAX_PACKED_ROWS 16        /* rows of one warp-MMA tile (P*G up to this) */
 #define IDX_WIDE_TILE_ROWS 128        /* rows of one tensor-core tile (P*G above 16) */
 #define IDX_MAX_ROWS_PER_REQUEST 32768 /* packed_queries * gqa of one request */
+#define IDX_MAX_CP_WORLD 8            /* context shards idx_topk_merge accepts */
 #define IDX_MAX_TOPK 256
 #define IDX_WORKSPACE_HEADER_BYTES 1024
 #define IDX_MAX_REQUESTS 2048  /* per idx_score_topk call (draft rows per per-row call) */
@@ -203,6 +204,60 @@ IDX_API int idx_score_topk_lse(const void* q, const float* q_scale, int q_dtype,
                                int init_blocks, int local_blocks, int topk,
                                int32_t* out_ids, float* out_scores,
                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * idx_score_local_blocks — the step over one context shard (indexer context
+ * parallelism: sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring for EAGLE
+ * verify rows", Motivation and Modifications 1, name the per-shard scorer
+ * score_local_blocks).  The rank holding the shard calls it; idx_topk_merge then
+ * combines every shard's list.
+ *
+ * The shard is global blocks [block_begin, block_begin + max_pages / 2) of every
+ * request: page_table[s][p] is the page of the request's global tokens
+ * (2 * block_begin + p) * 64 .. + 63, so max_pages must be even (whole 128-token
+ * blocks; a block never straddles two shards).  row_lens, init_blocks,
+ * local_blocks and topk are the row's global ones: the forced blocks and the number
+ * c of candidates to choose come from the row's own global block count.  Row i of
+ * request r gets the shard's forced blocks (ascending, global ids), then its best
+ * min(c, candidates in the shard) candidates by score (ties to the lower id), then
+ * (-1, -inf) pads.  Packed rows of one 16-row tile only (P*G <= 16).  Other
+ * arguments, the workspace (sized for the shard's max_pages) and the error
+ * behaviour are those of idx_score_topk; rows longer than the shard are not
+ * flagged (IDX_DEVERR_LEN_CLAMPED is for whole-context calls).
+ */
+IDX_API int idx_score_local_blocks(const void* q, const float* q_scale, int q_dtype,
+                                   const void* k_payload, const void* k_scale, int k_dtype,
+                                   int64_t num_pages, const int32_t* page_table, int n_slots,
+                                   int max_pages, int block_begin, const int32_t* slot_ids,
+                                   const int32_t* row_lens, int num_requests,
+                                   int packed_queries, int gqa, int init_blocks,
+                                   int local_blocks, int topk, int32_t* out_ids,
+                                   float* out_scores, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
+ * idx_topk_merge — the exchange step's re-selection: combine the lists of `world`
+ * context shards into each row's global selection.
+ *
+ *   cand_ids, cand_scores (device): int32 / fp32 [world][R][P*G][topk], shard w's
+ *                        idx_score_local_blocks output (any order of shards); the
+ *                        shards must partition every row's blocks
+ *   slot_ids, row_lens (device): as for idx_score_topk (global lengths; a slot
+ *                        outside [0, n_slots) makes the request's rows pads)
+ *   out_ids, out_scores (device): int32 / fp32 [R][P*G][topk]
+ * Row i gets its forced blocks ascending with the score their shard reported, then
+ * the best c of all the shards' other entries (score desc, ties to the lower id),
+ * then (-1, -inf) pads: the same as idx_score_topk over the whole context, since
+ * each shard keeps its best c candidates.  Host checks return IDX_ERR_INVALID
+ * (world outside [1, IDX_MAX_CP_WORLD], R outside [0, IDX_MAX_REQUESTS], P*G out of
+ * range, topk or init/local out of range, n_slots < 1, NULL pointers).
+ * Asynchronous on stream; allocates nothing.
+ */
+IDX_API int idx_topk_merge(const int32_t* cand_ids, const float* cand_scores, int world,
+                           const int32_t* slot_ids, const int32_t* row_lens, int n_slots,
+                           int num_requests, int packed_queries, int gqa, int init_blocks,
+                           int local_blocks, int topk, int32_t* out_ids, float* out_scores,
+                           void* stream);
 
 /*
  * idx_score_topk_perrow — the same step with every draft row scored as its own decode

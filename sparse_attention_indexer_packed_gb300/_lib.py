@@ -58,6 +58,9 @@ _SIGNATURES = {
                                 _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "idx_score_topk_perrow": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
                                    _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "idx_score_local_blocks": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _I, _P, _P, _I,
+                                    _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "idx_topk_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "idx_score_topk_noalloc": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
                                     _I, _I, _I, _I, _P, _P, _P]),
     "idx_set_kernel_events": (_I, [_P, _P, _P]),
@@ -211,6 +214,47 @@ def idx_score_topk_perrow(q, q_scale, k_payload, k_scale, k_dtype, page_table, s
     _score("idx_score_topk_perrow", q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids,
            row_lens, packed_queries, gqa, init_blocks, local_blocks, topk, out_ids, out_scores,
            workspace, stream)
+
+
+def idx_score_local_blocks(q, q_scale, k_payload, k_scale, k_dtype, page_table, block_begin,
+                           slot_ids, row_lens, packed_queries, gqa, init_blocks, local_blocks,
+                           topk, out_ids, out_scores, workspace, stream=None) -> None:
+    """One context shard: page_table [n_slots, max_pages] covers global blocks
+    [block_begin, block_begin + max_pages / 2) of every request."""
+    R = int(q.shape[0])
+    num_pages = int(k_payload.shape[0]) // PAGE
+    n_slots, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+    for t, name, dt in [(page_table, "page_table", torch.int32), (slot_ids, "slot_ids", torch.int32),
+                        (row_lens, "row_lens", torch.int32), (out_ids, "out_ids", torch.int32),
+                        (out_scores, "out_scores", torch.float32)]:
+        if t.dtype != dt:
+            raise IdxError(f"{name} must be {dt}")
+    rc = lib().idx_score_local_blocks(
+        _dev(q, "q"), _dev(q_scale, "q_scale", required=False), _q_dtype(q),
+        _dev(k_payload, "k_payload"), _dev(k_scale, "k_scale", required=False), DTYPES[k_dtype],
+        num_pages, _dev(page_table, "page_table"), n_slots, max_pages, int(block_begin),
+        _dev(slot_ids, "slot_ids"), _dev(row_lens, "row_lens"), R, packed_queries, gqa,
+        init_blocks, local_blocks, topk, _dev(out_ids, "out_ids"), _dev(out_scores, "out_scores"),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check(rc, "idx_score_local_blocks")
+
+
+def idx_topk_merge(cand_ids, cand_scores, slot_ids, row_lens, n_slots, packed_queries, gqa,
+                   init_blocks, local_blocks, topk, out_ids, out_scores, stream=None) -> None:
+    """cand_ids / cand_scores: [world, R, P*G, topk], the shards' lists."""
+    world, R = int(cand_ids.shape[0]), int(cand_ids.shape[1])
+    for t, name, dt in [(cand_ids, "cand_ids", torch.int32), (cand_scores, "cand_scores", torch.float32),
+                        (slot_ids, "slot_ids", torch.int32), (row_lens, "row_lens", torch.int32),
+                        (out_ids, "out_ids", torch.int32), (out_scores, "out_scores", torch.float32)]:
+        if t.dtype != dt:
+            raise IdxError(f"{name} must be {dt}")
+    rc = lib().idx_topk_merge(_dev(cand_ids, "cand_ids"), _dev(cand_scores, "cand_scores"), world,
+                              _dev(slot_ids, "slot_ids"), _dev(row_lens, "row_lens"), int(n_slots),
+                              R, packed_queries, gqa, init_blocks, local_blocks, topk,
+                              _dev(out_ids, "out_ids"), _dev(out_scores, "out_scores"),
+                              _stream_ptr(stream))
+    _check(rc, "idx_topk_merge")
 
 
 def idx_set_kernel_events(score_begin=None, score_end=None, topk_end=None) -> None:

@@ -187,7 +187,10 @@ int make_q_map(int q_dtype, const void* q, int64_t rows, CUtensorMap* map) {
   return IDX_OK;
 }
 
-int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_scale, int q_dtype,
+// block_begin < 0: the page table covers each request's whole context; >= 0:
+// it covers one context shard starting at that global block.
+int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q,
+                    const float* q_scale, int q_dtype,
                     const void* k_payload, const void* k_scale, int k_dtype, int64_t num_pages,
                     const int32_t* page_table, int n_slots, int max_pages, const int32_t* slot_ids,
                     const int32_t* row_lens, int R, int P, int G, int init_blocks,
@@ -201,6 +204,14 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
     return fail(IDX_ERR_INVALID, "per-row scoring needs gqa <= %d (got %d)", IDX_MAX_PACKED_ROWS,
                 G);
   const bool wide = !perrow && P * G > IDX_MAX_PACKED_ROWS;
+  const bool shard = block_begin >= 0;
+  if (shard && (perrow || wide))
+    return fail(IDX_ERR_INVALID,
+                "context-shard scoring takes packed rows of one 16-row tile (P*G <= 16)");
+  if (shard && (max_pages % 2 != 0 || block_begin > (1 << 24)))
+    return fail(IDX_ERR_INVALID,
+                "a context shard holds whole 128-token blocks: max_pages must be even (got %d)",
+                max_pages);
   const int tiles = (P * G + IDX_WIDE_TILE_ROWS - 1) / IDX_WIDE_TILE_ROWS;
   if (wide && (long long)R * tiles > idx::kMaxGroups)
     return fail(IDX_ERR_INVALID,
@@ -278,6 +289,8 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
   sa.M = P * G;
   sa.perrow = perrow ? 1 : 0;
   sa.tiles = tiles;
+  sa.block_off = shard ? block_begin : 0;
+  sa.shard = shard ? 1 : 0;
   CUtensorMap qmap = map;
   if (wide && k_dtype != IDX_NVFP4) {
     rc = make_q_map(q_dtype, q, (int64_t)R * P * G, &qmap);
@@ -309,6 +322,8 @@ int score_topk_impl(bool perrow, int block_score, const void* q, const float* q_
   ta.init_blocks = init_blocks;
   ta.local_blocks = local_blocks;
   ta.topk = topk;
+  ta.block_off = sa.block_off;
+  ta.shard = sa.shard;
   e = idx::launch_topk(ta, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the top-k kernel");
   if (ev[2] && (e = record_event(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
@@ -420,7 +435,7 @@ int idx_score_topk(const void* q, const float* q_scale, int q_dtype, const void*
                    int num_requests, int packed_queries, int gqa, int init_blocks,
                    int local_blocks, int topk, int32_t* out_ids, float* out_scores,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  return score_topk_impl(false, idx::kBlockMax, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
+  return score_topk_impl(false, idx::kBlockMax, -1, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
                          page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
                          packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
                          out_scores, workspace, workspace_bytes, stream);
@@ -433,7 +448,7 @@ int idx_score_topk_lse(const void* q, const float* q_scale, int q_dtype, const v
                        int packed_queries, int gqa, int init_blocks, int local_blocks, int topk,
                        int32_t* out_ids, float* out_scores, void* workspace,
                        size_t workspace_bytes, void* stream) {
-  return score_topk_impl(false, idx::kBlockLse, q, q_scale, q_dtype, k_payload, k_scale, k_dtype,
+  return score_topk_impl(false, idx::kBlockLse, -1, q, q_scale, q_dtype, k_payload, k_scale, k_dtype,
                          num_pages, page_table, n_slots, max_pages, slot_ids, row_lens,
                          num_requests, packed_queries, gqa, init_blocks, local_blocks, topk,
                          out_ids, out_scores, workspace, workspace_bytes, stream);
@@ -446,7 +461,7 @@ int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dtype, cons
                           int packed_queries, int gqa, int init_blocks, int local_blocks,
                           int topk, int32_t* out_ids, float* out_scores, void* workspace,
                           size_t workspace_bytes, void* stream) {
-  return score_topk_impl(true, idx::kBlockMax, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
+  return score_topk_impl(true, idx::kBlockMax, -1, q, q_scale, q_dtype, k_payload, k_scale, k_dtype, num_pages,
                          page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
                          packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
                          out_scores, workspace, workspace_bytes, stream);
@@ -479,6 +494,66 @@ int idx_workspace_errors(const void* workspace, void* stream, uint32_t* flags) {
   uint32_t f = 0;
   for (uint32_t c = 0; c < n; ++c) f |= header[idx::kFlagBytesOff + c];
   *flags = f;
+  return IDX_OK;
+}
+
+int idx_score_local_blocks(const void* q, const float* q_scale, int q_dtype,
+                           const void* k_payload, const void* k_scale, int k_dtype,
+                           int64_t num_pages, const int32_t* page_table, int n_slots,
+                           int max_pages, int block_begin, const int32_t* slot_ids,
+                           const int32_t* row_lens, int num_requests, int packed_queries, int gqa,
+                           int init_blocks, int local_blocks, int topk, int32_t* out_ids,
+                           float* out_scores, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (block_begin < 0)
+    return fail(IDX_ERR_INVALID, "block_begin must be >= 0 (got %d)", block_begin);
+  return score_topk_impl(false, idx::kBlockMax, block_begin, q, q_scale, q_dtype, k_payload,
+                         k_scale, k_dtype, num_pages, page_table, n_slots, max_pages, slot_ids,
+                         row_lens, num_requests, packed_queries, gqa, init_blocks, local_blocks,
+                         topk, out_ids, out_scores, workspace, workspace_bytes, stream);
+}
+
+int idx_topk_merge(const int32_t* cand_ids, const float* cand_scores, int world,
+                   const int32_t* slot_ids, const int32_t* row_lens, int n_slots,
+                   int num_requests, int packed_queries, int gqa, int init_blocks,
+                   int local_blocks, int topk, int32_t* out_ids, float* out_scores,
+                   void* stream) {
+  const int R = num_requests, P = packed_queries, G = gqa;
+  if (world < 1 || world > IDX_MAX_CP_WORLD)
+    return fail(IDX_ERR_INVALID, "world must be in [1, %d] (got %d)", IDX_MAX_CP_WORLD, world);
+  if (R < 0 || R > IDX_MAX_REQUESTS)
+    return fail(IDX_ERR_INVALID, "num_requests must be in [0, %d] (got %d)", IDX_MAX_REQUESTS, R);
+  if (P < 1 || G < 1 || (long long)P * G > IDX_MAX_ROWS_PER_REQUEST)
+    return fail(IDX_ERR_INVALID, "packed_queries * gqa must be in [1, %d] (got %d x %d)",
+                IDX_MAX_ROWS_PER_REQUEST, P, G);
+  if (topk < 1 || topk > IDX_MAX_TOPK)
+    return fail(IDX_ERR_INVALID, "topk must be in [1, %d] (got %d)", IDX_MAX_TOPK, topk);
+  if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > topk)
+    return fail(IDX_ERR_INVALID,
+                "need init_blocks, local_blocks >= 0 and init + local <= topk (got %d, %d, %d)",
+                init_blocks, local_blocks, topk);
+  if (n_slots < 1) return fail(IDX_ERR_INVALID, "n_slots must be >= 1 (got %d)", n_slots);
+  if (R > 0 && (!cand_ids || !cand_scores || !slot_ids || !row_lens || !out_ids || !out_scores))
+    return fail(IDX_ERR_INVALID, "a required pointer is NULL");
+  if (R == 0) return IDX_OK;
+  idx::MergeArgs m;
+  m.cand_ids = cand_ids;
+  m.cand_scores = cand_scores;
+  m.slot_ids = slot_ids;
+  m.row_lens = row_lens;
+  m.out_ids = out_ids;
+  m.out_scores = out_scores;
+  m.world = world;
+  m.n_slots = n_slots;
+  m.R = R;
+  m.P = P;
+  m.G = G;
+  m.M = P * G;
+  m.init_blocks = init_blocks;
+  m.local_blocks = local_blocks;
+  m.topk = topk;
+  cudaError_t e = idx::launch_merge(m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the merge kernel");
   return IDX_OK;
 }
 

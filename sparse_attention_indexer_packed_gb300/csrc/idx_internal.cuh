@@ -53,6 +53,8 @@ struct ScoreArgs {
   int R, P, G, M;
   int perrow;                  // 0: groups are requests; 1: groups are draft rows
   int tiles;                   // wide path: 128-row tiles per request (groups = R * tiles)
+  int block_off;               // global block of local block 0 (a context shard); 0 otherwise
+  int shard;                   // 1: the page table holds one context shard of each request
 };
 
 struct TopkArgs {
@@ -64,6 +66,21 @@ struct TopkArgs {
   uint32_t* sched_counter;     // reset to zero for the next call
   unsigned long long* sched_tag;
   int n_slots, max_pages, nb_cap;
+  int R, P, G, M;
+  int init_blocks, local_blocks, topk;
+  int block_off;               // first global block the workspace's block 0 stands for
+  int shard;                   // 1: select within the shard [block_off, block_off + nb_cap)
+};
+
+// Merge of context shards' candidate lists: cand_* are [world][R*M][topk].
+struct MergeArgs {
+  const int32_t* cand_ids;
+  const float* cand_scores;
+  const int32_t* slot_ids;
+  const int32_t* row_lens;
+  int32_t* out_ids;
+  float* out_scores;
+  int world, n_slots;
   int R, P, G, M;
   int init_blocks, local_blocks, topk;
 };
@@ -137,6 +154,7 @@ cudaError_t launch_wide(int key_format, int block_score, const ScoreArgs& args,
                         const CUtensorMap& payload_map, const CUtensorMap& q_map,
                         cudaStream_t stream);
 cudaError_t launch_topk(const TopkArgs& args, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& args, cudaStream_t stream);
 cudaError_t launch_store_nvfp4(const uint16_t* src, const int64_t* slot_mapping, int64_t num_tokens,
                                uint8_t* payload, uint8_t* scale, int64_t num_rows,
                                cudaStream_t stream);

@@ -104,6 +104,12 @@ __device__ __forceinline__ int clamp_len(int L, int max_tokens) {
   return L > max_tokens ? max_tokens : L;
 }
 
+// Tokens the page table reaches, counted from the start of the context: a
+// context shard's table begins at global block block_off.
+__device__ __forceinline__ int token_cap(const ScoreArgs& a) {
+  return (2 * a.block_off + a.max_pages) * kPage;
+}
+
 // Geometry of scoring group v (a request when packed, a draft row when per-row).
 __device__ Group group_info(const ScoreArgs& a, int v) {
   Group g;
@@ -122,16 +128,17 @@ __device__ Group group_info(const ScoreArgs& a, int v) {
   }
   g.slot = __ldg(a.slot_ids + g.r);
   const bool pad = g.slot < 0 || g.slot >= a.n_slots;
-  ext = clamp_len(ext, a.max_pages * kPage);
+  ext = clamp_len(ext, token_cap(a));
   g.extent = pad ? 0 : max(ext, 0);
-  g.nbk = (g.extent + kBlock - 1) / kBlock;
+  // blocks held here: global blocks [block_off, ceil(extent / 128)), local from 0
+  g.nbk = max(0, (g.extent + kBlock - 1) / kBlock - a.block_off);
   return g;
 }
 
 // Length of tile row i of group v (clamped; <= 0 means the row is empty).
 __device__ __forceinline__ int tile_row_len(const ScoreArgs& a, int v, int r, int i) {
   const int L = a.perrow ? __ldg(a.row_lens + v) : __ldg(a.row_lens + r * a.P + i / a.G);
-  return clamp_len(L, a.max_pages * kPage);
+  return clamp_len(L, token_cap(a));
 }
 
 // Scores are finite, so the max needs no NaN rule of its own: fmaxf is a single
@@ -572,9 +579,9 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       if (v < V) {
         const Group gi = group_info(a, v);
         nbk = gi.nbk;
-        const int rem = gi.extent - (nbk - 1) * kBlock;  // tokens in the last block
+        const int rem = gi.extent - (a.block_off + nbk - 1) * kBlock;  // tokens in the last block
         word = (nbk > 0 ? gi.slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
-        if (blockIdx.x == 0 && gi.slot >= 0 && gi.slot < a.n_slots) {
+        if (blockIdx.x == 0 && !a.shard && gi.slot >= 0 && gi.slot < a.n_slots) {
           const int j0 = a.perrow ? v - gi.r * a.P : 0, j1 = a.perrow ? j0 + 1 : a.P;
           for (int j = j0; j < j1; ++j)
             clamped |= __ldg(a.row_lens + gi.r * a.P + j) > a.max_pages * kPage;
@@ -691,7 +698,7 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       break;
     }
     __syncwarp();
-    const int tbase = b_cur * kBlock;
+    const int tbase = (a.block_off + b_cur) * kBlock;  // global token of the block
     Score score(qt.post_scale());
     // most blocks lie inside every live row: score them without the mask
     const bool whole = __all_sync(0xffffffffu, (row0 < 0 || tbase + kBlock <= L0) &&

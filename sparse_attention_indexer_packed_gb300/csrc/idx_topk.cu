@@ -28,6 +28,7 @@ namespace idx {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxWorld = 8;  // context shards a merge accepts
 constexpr int kWarps = kThreads / 32;
 constexpr int kBatch = 16;  // independent loads in flight per thread
 // The exact step ranks at most kCap entries (kCap >= the largest topk).
@@ -46,6 +47,42 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // composite sort key: larger score first, then lower id first
 __device__ __forceinline__ unsigned long long pack(uint32_t key, int id) {
   return ((unsigned long long)key << 32) | (uint32_t)(0x7fffffff - id);
+}
+
+// What a row selects: forced blocks [0, fi) and [ls, nb) and c more from the
+// candidates [fi, ls), all counted from the row's own global block count nb.
+// A context shard holds global blocks [s0, s1); it emits the forced blocks it
+// holds (nf of them, ascending: the part of [0, fi) it holds, then of
+// [ls, nb)), then its best min(c, its candidates) candidates from [cb,
+// cb + ncand).  The whole context is the shard [0, nb).
+struct RowPlan {
+  int nb, fi, ls, s0, s1, nf, cb, ncand, c;
+  __device__ int forced_id(int t) const {  // t < nf
+    const int n0 = max(0, min(fi, s1) - s0);
+    return t < n0 ? s0 + t : max(ls, s0) + (t - n0);
+  }
+};
+
+__device__ __forceinline__ RowPlan row_plan(const TopkArgs& a, int r, int i) {
+  RowPlan p;
+  const int slot = __ldg(a.slot_ids + r);
+  int L = 0;
+  if (slot >= 0 && slot < a.n_slots) {
+    L = __ldg(a.row_lens + r * a.P + i / a.G);
+    if (!a.shard) L = min(L, a.max_pages * kPage);  // a whole-context table caps the row
+  }
+  p.nb = L > 0 ? (L + kBlock - 1) / kBlock : 0;
+  p.fi = min(a.init_blocks, p.nb);
+  p.ls = max(p.fi, p.nb - a.local_blocks);
+  const int nf_all = p.fi + (p.nb - p.ls);
+  const int c_all = min(a.topk, p.nb) - nf_all;
+  p.s0 = a.shard ? a.block_off : 0;
+  p.s1 = a.shard ? min(p.nb, a.block_off + a.nb_cap) : p.nb;
+  p.nf = max(0, min(p.fi, p.s1) - p.s0) + max(0, p.s1 - max(p.ls, p.s0));
+  p.cb = max(p.fi, p.s0);
+  p.ncand = max(0, min(p.ls, p.s1) - p.cb);
+  p.c = min(c_all, p.ncand);
+  return p;
 }
 
 struct Shared {
@@ -74,15 +111,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
   float* out_sc = a.out_scores + (size_t)row * a.topk;
   const float* bm = a.blockmax + (size_t)row * a.nb_cap;
 
-  const int slot = __ldg(a.slot_ids + r);
-  int L = 0;
-  if (slot >= 0 && slot < a.n_slots) L = min(__ldg(a.row_lens + r * a.P + i / a.G), a.max_pages * kPage);
-  const int nb = L > 0 ? (L + kBlock - 1) / kBlock : 0;
-  const int fi = min(a.init_blocks, nb);       // forced init: [0, fi)
-  const int ls = max(fi, nb - a.local_blocks);  // forced local: [ls, nb)
-  const int nf = fi + (nb - ls);
-  const int ncand = ls - fi;                    // candidates: [fi, ls)
-  const int c = min(a.topk, nb) - nf;           // candidates to choose
+  const RowPlan pl = row_plan(a, r, i);
+  const int nf = pl.nf, ncand = pl.ncand, c = pl.c;
+  const int fi = pl.cb;  // global id of the first candidate
+  // the workspace holds this row's blocks from s0 on: block g at g - s0
+  const float* bmg = bm - pl.s0;
 
   // pads need no block maxima: write them before waiting on the score kernel
   for (int t = nf + max(c, 0) + tid; t < a.topk; t += kThreads) {
@@ -98,9 +131,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     *reinterpret_cast<volatile unsigned long long*>(a.sched_tag) = kSchedTag;
   }
   for (int t = tid; t < nf; t += kThreads) {
-    const int id = t < fi ? t : ls + (t - fi);
+    const int id = pl.forced_id(t);
     out_ids[t] = id;
-    out_sc[t] = bm[id];
+    out_sc[t] = bmg[id];
   }
   if (c <= 0) return;
 
@@ -111,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int t = t0 + u * kThreads + tid;
-      v[u] = t < ncand ? bm[fi + t] : 0.f;
+      v[u] = t < ncand ? bmg[fi + t] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -299,15 +332,11 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkA
   float* out_sc = a.out_scores + (size_t)row * a.topk;
   const float* bm = a.blockmax + (size_t)row * a.nb_cap;
 
-  const int slot = __ldg(a.slot_ids + r);
-  int L = 0;
-  if (slot >= 0 && slot < a.n_slots) L = min(__ldg(a.row_lens + r * a.P + i / a.G), a.max_pages * kPage);
-  const int nb = L > 0 ? (L + kBlock - 1) / kBlock : 0;
-  const int fi = min(a.init_blocks, nb);       // forced init: [0, fi)
-  const int ls = max(fi, nb - a.local_blocks);  // forced local: [ls, nb)
-  const int nf = fi + (nb - ls);
-  const int ncand = ls - fi;                    // candidates: [fi, ls)
-  const int c = min(a.topk, nb) - nf;           // candidates to choose
+  const RowPlan pl = row_plan(a, r, i);
+  const int nf = pl.nf, ncand = pl.ncand, c = pl.c;
+  const int fi = pl.cb;  // global id of the first candidate
+  // the workspace holds this row's blocks from s0 on: block g at g - s0
+  const float* bmg = bm - pl.s0;
 
   for (int t = nf + max(c, 0) + lane; t < a.topk; t += 32) {
     out_ids[t] = -1;
@@ -320,9 +349,9 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkA
     *reinterpret_cast<volatile unsigned long long*>(a.sched_tag) = kSchedTag;
   }
   for (int t = lane; t < nf; t += 32) {
-    const int id = t < fi ? t : ls + (t - fi);
+    const int id = pl.forced_id(t);
     out_ids[t] = id;
-    out_sc[t] = bm[id];
+    out_sc[t] = bmg[id];
   }
   if (c <= 0) return;
 
@@ -332,7 +361,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkA
   for (int q = 0; q < R; ++q) {
     const int e = lane + 32 * q;
     act[q] = e < ncand;
-    key[q] = act[q] ? order_key(bm[fi + e]) : 0u;
+    key[q] = act[q] ? order_key(bmg[fi + e]) : 0u;
   }
   bool sel[R];
 #pragma unroll
@@ -459,6 +488,102 @@ cudaError_t launch_topk_warp(const TopkArgs& a, int rows, cudaStream_t stream) {
                     32 * kRowsPerCta, 0, stream, a);
 }
 
+// ---------------------------------------------------------------------------
+// Merge of context shards' lists (indexer context parallelism, the exchange
+// step after each rank scored its shard; sglang #42614 names the per-shard
+// scorer score_local_blocks).  One warp per row, four rows per CTA.  Each
+// shard's list is its forced blocks, then its chosen candidates in (score desc,
+// id asc) order, then pads; a forced block goes straight to its slot in the
+// row's forced order, and a candidate's place among all shards' candidates is
+// its place in its own list plus, for every other shard, how many of that
+// shard's candidates rank above it (binary search, the lists being sorted).
+// Candidates placed c or later are dropped.  The shards must partition the
+// row's blocks, so each forced block appears in exactly one list.
+// ---------------------------------------------------------------------------
+constexpr int kMergeRowsPerCta = 4;
+
+__global__ void __launch_bounds__(32 * kMergeRowsPerCta) merge_kernel(const MergeArgs a) {
+  __shared__ int sh_nf[kMergeRowsPerCta][kMaxWorld];
+  __shared__ int sh_nc[kMergeRowsPerCta][kMaxWorld];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows = a.R * a.M;
+  const int row = blockIdx.x * kMergeRowsPerCta + warp;
+  if (row >= rows) return;
+  const int r = row / a.M;
+  const int i = row - r * a.M;
+  const int slot = __ldg(a.slot_ids + r);
+  const int L = (slot >= 0 && slot < a.n_slots) ? __ldg(a.row_lens + r * a.P + i / a.G) : 0;
+  const int nb = L > 0 ? (L + kBlock - 1) / kBlock : 0;
+  const int fi = min(a.init_blocks, nb);
+  const int ls = max(fi, nb - a.local_blocks);
+  const int nf = fi + (nb - ls);
+  const int c = min(a.topk, nb) - nf;
+  int32_t* out_ids = a.out_ids + (size_t)row * a.topk;
+  float* out_sc = a.out_scores + (size_t)row * a.topk;
+  for (int t = lane; t < a.topk; t += 32) {
+    out_ids[t] = -1;
+    out_sc[t] = -INFINITY;
+  }
+  // the lists are written by the shards' top-k (or copied in by the exchange)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  auto ids_of = [&](int w) { return a.cand_ids + ((size_t)w * rows + row) * a.topk; };
+  auto sc_of = [&](int w) { return a.cand_scores + ((size_t)w * rows + row) * a.topk; };
+  auto forced = [&](int id) { return id < fi || (id >= ls && id < nb); };
+  for (int w = 0; w < a.world; ++w) {
+    const int32_t* ids = ids_of(w);
+    int nfw = 0, ncw = 0;
+    for (int p = lane; p < a.topk; p += 32) {
+      const int id = ids[p];
+      if (id >= 0) {
+        if (forced(id)) ++nfw;
+        else ++ncw;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      nfw += __shfl_xor_sync(0xffffffffu, nfw, o);
+      ncw += __shfl_xor_sync(0xffffffffu, ncw, o);
+    }
+    if (lane == 0) {
+      sh_nf[warp][w] = nfw;
+      sh_nc[warp][w] = ncw;
+    }
+  }
+  __syncwarp();  // the pads above are written, the list sizes visible
+  for (int e = lane; e < a.world * a.topk; e += 32) {
+    const int w = e / a.topk, p = e - w * a.topk;
+    const int id = ids_of(w)[p];
+    if (id < 0) continue;
+    const float v = sc_of(w)[p];
+    if (forced(id)) {
+      const int pos = id < fi ? id : fi + (id - ls);
+      out_ids[pos] = id;
+      out_sc[pos] = v;
+      continue;
+    }
+    const unsigned long long x = pack(order_key(v), id);
+    int rank = p - sh_nf[warp][w];
+    for (int w2 = 0; w2 < a.world; ++w2) {
+      if (w2 == w) continue;
+      const int32_t* ids2 = ids_of(w2);
+      const float* sc2 = sc_of(w2);
+      int lo = sh_nf[warp][w2], hi = lo + sh_nc[warp][w2];
+      const int base = lo;
+      while (lo < hi) {  // first entry not above x (the list is descending)
+        const int mid = (lo + hi) >> 1;
+        if (pack(order_key(sc2[mid]), ids2[mid]) > x) lo = mid + 1;
+        else hi = mid;
+      }
+      rank += lo - base;
+    }
+    if (rank < c) {
+      out_ids[nf + rank] = id;
+      out_sc[nf + rank] = v;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
@@ -493,6 +618,16 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, topk_kernel, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+  const int rows = a.R * a.M;
+  if (rows == 0) return cudaSuccess;
+  if (a.world < 1 || a.world > kMaxWorld) return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(merge_kernel, (rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta,
+                             32 * kMergeRowsPerCta, 0, stream, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
