@@ -175,7 +175,7 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  * Asynchronous on stream; allocates nothing; capturable in a CUDA graph.
  * Host-side checks return IDX_ERR_INVALID (P*G outside [1, IDX_MAX_ROWS_PER_REQUEST],
  * topk out of range, init+local > topk, NULL pointers, R < 0 or > IDX_MAX_REQUESTS,
- * R * ceil(P*G / IDX_WIDE_TILE_ROWS) > IDX_MAX_REQUESTS when P*G > 16, n_slots or
+ * R * ceil(ceil(P*G / IDX_WIDE_TILE_ROWS) / 2) > IDX_MAX_REQUESTS when P*G > 16, n_slots or
  * max_pages < 1, workspace too
  * small or misaligned, num_pages < 1).  With R == 0 only the workspace is required
  * (its header is reset) and the per-request pointers may be NULL.

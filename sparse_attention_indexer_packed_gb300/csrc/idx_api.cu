@@ -213,11 +213,11 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
                 "a context shard holds whole 128-token blocks: max_pages must be even (got %d)",
                 max_pages);
   const int tiles = (P * G + IDX_WIDE_TILE_ROWS - 1) / IDX_WIDE_TILE_ROWS;
-  if (wide && (long long)R * tiles > idx::kMaxGroups)
+  if (wide && (long long)R * ((tiles + 1) / 2) > idx::kMaxGroups)
     return fail(IDX_ERR_INVALID,
-                "at most %d request tiles per call (num_requests * ceil(packed_queries * gqa / "
-                "%d) = %lld)",
-                idx::kMaxGroups, IDX_WIDE_TILE_ROWS, (long long)R * tiles);
+                "at most %d pairs of request tiles per call (num_requests * ceil(packed_queries "
+                "* gqa / %d) / 2, rounded up per request, = %lld)",
+                idx::kMaxGroups, IDX_WIDE_TILE_ROWS, (long long)R * ((tiles + 1) / 2));
   if (topk < 1 || topk > IDX_MAX_TOPK)
     return fail(IDX_ERR_INVALID, "topk must be in [1, %d] (got %d)", IDX_MAX_TOPK, topk);
   if (init_blocks < 0 || local_blocks < 0 || init_blocks + local_blocks > topk)

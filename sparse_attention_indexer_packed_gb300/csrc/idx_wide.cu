@@ -3,9 +3,10 @@
 // position -- on the 5th-generation tensor cores.
 //
 // The rows of a request are cut into tiles of up to 128 (tile tau holds rows
-// [128 tau, 128 tau + 128)); each tile is one "group" that streams the request's
-// keys once.  A 128-row x 128-token x 128-dim product is one tcgen05.mma chain
-// (M = 128, N = 128) accumulating in fp32 in tensor memory, so the dot work of
+// [128 tau, 128 tau + 128)), and tiles 2p and 2p + 1 form one "group" that
+// streams the request's keys once for both.  A 128-row x 128-token x 128-dim
+// product is one tcgen05.mma chain (M = 128, N = 128) accumulating in fp32 in
+// tensor memory, so the dot work of
 // the pages' per-request dot tile (sglang #45451, Modifications: the draft rows of
 // a request share one dot tile against its index K) is done for 128 rows at a
 // time instead of 16.  Each row keeps its own length mask and its block max (or
@@ -14,19 +15,19 @@
 //
 // Roles inside a CTA (one CTA per SM, persistent over a contiguous range of
 // blocks of the flattened (group, block) list):
-//   warp 0      TMA producer: the group's query tile (bf16 / e4m3) and each
+//   warp 0      TMA producer: the group's query tiles (bf16 / e4m3) and each
 //               block's two key pages (+ their scales) into a ring of stages;
-//   warp 1      allocates 512 TMEM columns (a ring of four 128-column fp32
-//               accumulators); lane 0 issues the MMAs of a block and commits
+//   warp 1      allocates 512 TMEM columns (one 128-column fp32 accumulator
+//               per tile of a pair, two blocks in flight); lane 0 issues both
+//               tiles' MMAs of a block against the same staged keys and commits
 //               them to mbarriers;
-//   warps 2..9  epilogue, two groups of four warps taking alternate blocks:
+//   warps 2..9  epilogue, group g (four warps) owning tile g of the pair:
 //               thread = tile row; tcgen05.ld of its 128 scores, the row's mask
 //               and block score, one workspace write per row;
 //   warps 10..13 (NVFP4 keys) decode a block's e2m1 codes x E4M3 group scales
 //               into an f16 operand tile (ROCm/ATOM #2745: the products are
-//               exact); the first epilogue group also converts the bf16 query
-//               tile to f16 with a per-row power-of-two scale, undone on the
-//               result.
+//               exact); each epilogue group also converts its bf16 query tile
+//               to f16 with a per-row power-of-two scale, undone on the result.
 // Every wait is bounded; a timeout sets IDX_DEVERR_TIMEOUT and the CTA winds down
 // (copies in flight are waited for, TMEM is freed).
 #include <cuda_bf16.h>
@@ -44,8 +45,9 @@ namespace idx {
 namespace {
 
 constexpr int kWRows = 128;     // tile rows (MMA M)
-constexpr int kAcc = 4;          // fp32 accumulators of 128 columns in the TMEM ring
-constexpr int kTmemCols = 128 * kAcc;
+constexpr int kPair = 2;         // tiles of one request that share a key block
+constexpr int kUnits = 2;        // blocks in flight in tensor memory
+constexpr int kTmemCols = 128 * kPair * kUnits;  // one 128-column fp32 accumulator per tile
 constexpr unsigned int kErrBadPage = 1u;  // IDX_DEVERR_BAD_PAGE
 constexpr unsigned int kErrTimeout = 2u;  // IDX_DEVERR_TIMEOUT
 constexpr unsigned int kErrLenClamped = 4u;  // IDX_DEVERR_LEN_CLAMPED
@@ -54,18 +56,18 @@ template <int KF>
 struct WCfg;
 template <>
 struct WCfg<kBf16> {
-  static constexpr int kQBytes = 32768;     // 128 rows x 256 B: two 16 KB K-halves
+  static constexpr int kQBytes = 32768;     // one tile: 128 rows x 256 B, two 16 KB K-halves
   static constexpr int kStageBytes = 32768; // 128 tokens x 256 B: two 16 KB K-halves
   static constexpr int kPagePayload = 16384;
   static constexpr int kPageScale = 0;
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 4;
   static constexpr int kDecStages = 0;
   static constexpr int kDecWarps = 0;
   static constexpr uint32_t kIdesc = instr_desc(1u, 128, 128);  // bf16 x bf16
 };
 template <>
 struct WCfg<kFp8> {
-  static constexpr int kQBytes = 16384;     // 128 rows x 128 B
+  static constexpr int kQBytes = 16384;     // one tile: 128 rows x 128 B
   static constexpr int kStageBytes = 16384; // 128 tokens x 128 B
   static constexpr int kPagePayload = 8192;
   static constexpr int kPageScale = 256;    // 64 fp32
@@ -76,11 +78,11 @@ struct WCfg<kFp8> {
 };
 template <>
 struct WCfg<kNvfp4> {
-  static constexpr int kQBytes = 32768;     // f16 query tile
+  static constexpr int kQBytes = 32768;     // one f16 query tile
   static constexpr int kStageBytes = 8192;  // raw codes of 128 tokens (64 B each)
   static constexpr int kPagePayload = 4096;
   static constexpr int kPageScale = 512;    // 64 x 8 E4M3 bytes
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 4;
   static constexpr int kDecStages = 3;      // decoded f16 tiles, 32 KB each
   static constexpr int kDecWarps = 4;
   static constexpr uint32_t kIdesc = instr_desc(0u, 128, 128);  // f16 x f16
@@ -91,13 +93,13 @@ struct WLayout {
   using C = WCfg<KF>;
   static constexpr int S = C::kStages;
   static constexpr int SD = C::kDecStages;
-  static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQOff + C::kQBytes;
+  static constexpr int kQOff = 0;  // kPair query tiles
+  static constexpr int kStageOff = kQOff + kPair * C::kQBytes;
   static constexpr int kDecOff = kStageOff + S * C::kStageBytes;
   static constexpr int kScaleOff = kDecOff + SD * 32768;
   static constexpr int kBarOff = kScaleOff + S * 2 * C::kPageScale;
-  // full[S] empty[S] dfull[SD] dempty[SD] afull[kAcc] aempty[kAcc] qfull qempty done
-  static constexpr int kNumBars = 2 * S + 2 * SD + 2 * kAcc + 3;
+  // full[S] empty[S] dfull[SD] dempty[SD] afull[kUnits] aempty[kUnits] qfull qempty done
+  static constexpr int kNumBars = 2 * S + 2 * SD + 2 * kUnits + 3;
   static constexpr int kCtlOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kGroupOff = kCtlOff + 64;
   static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
@@ -121,16 +123,16 @@ struct WLayout {
     return sb + kBarOff + 8 * (2 * S + 2 * SD + j);
   }
   __device__ static uint32_t aempty(uint32_t sb, int j) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + kAcc + j);
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + kUnits + j);
   }
   __device__ static uint32_t qfull(uint32_t sb) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kAcc);
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits);
   }
   __device__ static uint32_t qempty(uint32_t sb) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kAcc + 1);
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + 1);
   }
   __device__ static uint32_t done(uint32_t sb) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kAcc + 2);
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + 2);
   }
 };
 
@@ -339,19 +341,19 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(L::full(sb, s), 1);
-      // who frees a raw stage: the MMA (bf16), the MMA and the four epilogue
+      // who frees a raw stage: the MMA (bf16), the MMA and the eight epilogue
       // warps that read its key scales (fp8), the four decoder warps (NVFP4)
-      mbar_init(L::empty(sb, s), KF == kBf16 ? 1 : (KF == kFp8 ? 5 : 4));
+      mbar_init(L::empty(sb, s), KF == kBf16 ? 1 : (KF == kFp8 ? 9 : 4));
     }
     for (int d = 0; d < SD; ++d) {
       mbar_init(L::dfull(sb, d), C::kDecWarps);
       mbar_init(L::dempty(sb, d), 1);
     }
-    for (int j = 0; j < kAcc; ++j) {
+    for (int j = 0; j < kUnits; ++j) {
       mbar_init(L::afull(sb, j), 1);
-      mbar_init(L::aempty(sb, j), 4);
+      mbar_init(L::aempty(sb, j), 8);  // both epilogue groups, every block
     }
-    mbar_init(L::qfull(sb), KF == kNvfp4 ? 4 : 1);
+    mbar_init(L::qfull(sb), KF == kNvfp4 ? 8 : 1);
     mbar_init(L::qempty(sb), 1);
     mbar_init(L::done(sb), 1);
     fence_barrier_init();
@@ -368,11 +370,14 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
   // the workspace written, so wait for that work to complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- group table: block prefix sums and slots of every (request, tile) ----
+  // ---- group table: block prefix sums and slots of every (request, tile pair)
+  // group v = (request v / TP, tiles 2 (v % TP) and 2 (v % TP) + 1): TP pairs
+  // per request, the last a single tile when a request has an odd count
   // (1) every thread takes draft rows: a tile's extent is the longest of the
   // draft rows any of its rows belongs to (one load per draft row, all in flight
   // at once); (2) warp 0 turns extents into block counts and prefix sums.
-  const int V = a.R * a.tiles;
+  const int TP = (a.tiles + 1) / 2;
+  const int V = a.R * TP;
   for (int v = threadIdx.x; v < V; v += blockDim.x) gpre[v] = 0;
   if (threadIdx.x == 0) *cta_flags = 0u;
   __syncthreads();
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       if (L <= 0) continue;
       const int r = x / a.P, j = x - r * a.P;
       const int t0 = (j * a.G) / kWRows, t1 = (j * a.G + a.G - 1) / kWRows;
-      for (int t = t0; t <= t1; ++t) atomicMax(&gpre[r * a.tiles + t], min(L, cap));
+      for (int t = t0 / 2; t <= t1 / 2; ++t) atomicMax(&gpre[r * TP + t], min(L, cap));
       if (blockIdx.x == 0 && L > cap) {
         const int slot = __ldg(a.slot_ids + r);
         clamped |= slot >= 0 && slot < a.n_slots;
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       int nbk = 0, word = 0;
       if (v < V) {
         const int ext = gpre[v];
-        const int slot = __ldg(a.slot_ids + v / a.tiles);
+        const int slot = __ldg(a.slot_ids + v / TP);
         const bool pad = slot < 0 || slot >= a.n_slots;
         nbk = (pad || ext <= 0) ? 0 : (ext + kBlock - 1) / kBlock;
         const int rem = ext - (nbk - 1) * kBlock;  // tokens in the last block
@@ -457,17 +462,22 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       const int p1 = __shfl_sync(0xffffffffu, wpg, 2 * k + 1);
       if (v != prev_v) {
         if (KF != kNvfp4 && lane == 0) {
-          // the previous tile's MMAs must be done with the query tile
+          // the previous pair's MMAs must be done with the query tiles
           if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
           if (ok) {
-            const int r = v / a.tiles;
-            const int base_row = r * a.M + (v - r * a.tiles) * kWRows;
-            mbar_arrive_expect_tx(L::qfull(sb), C::kQBytes);
-            if (KF == kBf16) {
-              tma_load_2d(qtile, &qmap, 0, base_row, L::qfull(sb));
-              tma_load_2d(qtile + 16384, &qmap, 64, base_row, L::qfull(sb));
-            } else {
-              tma_load_2d(qtile, &qmap, 0, base_row, L::qfull(sb));
+            const int r = v / TP;
+            const int tile0 = 2 * (v - r * TP);
+            const int nt = min(kPair, a.tiles - tile0);
+            mbar_arrive_expect_tx(L::qfull(sb), nt * C::kQBytes);
+            for (int t = 0; t < nt; ++t) {
+              const int base_row = r * a.M + (tile0 + t) * kWRows;
+              const uint32_t qt = qtile + t * C::kQBytes;
+              if (KF == kBf16) {
+                tma_load_2d(qt, &qmap, 0, base_row, L::qfull(sb));
+                tma_load_2d(qt + 16384, &qmap, 64, base_row, L::qfull(sb));
+              } else {
+                tma_load_2d(qt, &qmap, 0, base_row, L::qfull(sb));
+              }
             }
           }
         }
@@ -517,7 +527,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      int prev_v = -1, nq = 0, i = 0;
+      int prev_v = -1, nq = 0, i = 0, nt = 1;
       bool ok = true;
       int v = 0, b = 0;
       if (u0 < u1) wlocate(gpre, V, u0, v, b);
@@ -526,6 +536,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
           if (!mbar_wait_bounded(L::qfull(sb), nq & 1)) { ok = false; break; }
           ++nq;
           prev_v = v;
+          nt = min(kPair, a.tiles - 2 * (v % TP));
         }
         const int s = i % S;
         uint32_t opnd;
@@ -537,21 +548,25 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
           if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1)) { ok = false; break; }
           opnd = sb + L::kStageOff + s * C::kStageBytes;
         }
-        const int j = i % kAcc;
-        if (i >= kAcc && !mbar_wait_bounded(L::aempty(sb, j), ((i / kAcc) - 1) & 1)) { ok = false; break; }
+        const int j = i % kUnits;
+        if (i >= kUnits && !mbar_wait_bounded(L::aempty(sb, j), ((i / kUnits) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(j * 128);
-        if (KF == kFp8) {
+        // both tiles of the pair against the same staged keys
+        for (int t = 0; t < nt; ++t) {
+          const uint32_t d_tmem = tmem + (uint32_t)((j * kPair + t) * 128);
+          const uint32_t qt = qtile + t * C::kQBytes;
+          if (KF == kFp8) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma_f8(d_tmem, desc_kmajor_sw128(qtile + ks * 32), desc_kmajor_sw128(opnd + ks * 32),
-                      C::kIdesc, ks > 0 ? 1u : 0u);
-        } else {
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_f8(d_tmem, desc_kmajor_sw128(qt + ks * 32), desc_kmajor_sw128(opnd + ks * 32),
+                        C::kIdesc, ks > 0 ? 1u : 0u);
+          } else {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
-            tc_mma_f16(d_tmem, desc_kmajor_sw128(qtile + off), desc_kmajor_sw128(opnd + off),
-                       C::kIdesc, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
+              tc_mma_f16(d_tmem, desc_kmajor_sw128(qt + off), desc_kmajor_sw128(opnd + off),
+                         C::kIdesc, ks > 0 ? 1u : 0u);
+            }
           }
         }
         if constexpr (KF == kNvfp4) tc_commit(L::dempty(sb, i % SD));
@@ -560,7 +575,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         int vn = v, bn = b;
         if (u + 1 < u1) wnext(gpre, V, vn, bn);
         else vn = -1;
-        if (vn != v) tc_commit(L::qempty(sb));  // last block of this tile
+        if (vn != v) tc_commit(L::qempty(sb));  // last block of this pair
         v = vn;
         b = bn;
       }
@@ -572,73 +587,77 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     __syncwarp();
   } else if (warp < L::kDecWarp0) {
     // ======================= epilogue =======================
-    // group eg takes the blocks with i % 2 == eg (accumulators eg, eg + 2); both
-    // groups walk every block to follow the tiles
+    // group eg owns tile eg of each pair (accumulator j * kPair + eg of block i,
+    // j = i % kUnits); it waits for and frees every block's accumulators, also
+    // when its pair has a single tile, so the barrier phases stay in step
     const int eg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int ti = quarter * 32 + lane;  // tile row of this thread
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     int prev_v = -1, nq = 0, i = 0;
     int Lrow = 0, out_row = -1;
+    bool mine = false;  // the current pair has a tile eg
     float post = 1.f, qs = 0.f;
     bool ok = true;
     int v = 0, b = 0;
     if (u0 < u1) wlocate(gpre, V, u0, v, b);
     for (int u = u0; u < u1; ++u, ++i, wnext(gpre, V, v, b)) {
       if (v != prev_v) {
-        const int r = v / a.tiles;
-        const int row0 = (v - r * a.tiles) * kWRows;
-        const int nrows = min(kWRows, a.M - row0);
+        const int r = v / TP;
+        const int tile = 2 * (v - r * TP) + eg;
+        mine = tile < a.tiles;
+        const int row0 = tile * kWRows;
+        const int nrows = mine ? min(kWRows, a.M - row0) : 0;
         const bool live = ti < nrows && gpre[v + 1] > gpre[v];
         out_row = live ? r * a.M + row0 + ti : -1;
         Lrow = live ? min(__ldg(a.row_lens + r * a.P + (row0 + ti) / a.G), a.max_pages * kPage) : 0;
         if (KF == kFp8) qs = live ? __ldg(a.q_scale + out_row) : 0.f;
         if (KF == kNvfp4) {
-          // group 0 writes the f16 query tile once every MMA of the previous
-          // tile has completed; group 1 only derives its rows' scales
-          if (eg == 0 && nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
+          // each group writes its own f16 query tile once every MMA of the
+          // previous pair has completed
+          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
           if (!__all_sync(0xffffffffu, ok)) break;
-          post = convert_q_row(a, qtile, ti, r * a.M + row0, nrows, eg == 0);
-          if (eg == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(L::qfull(sb));
-          }
+          if (mine) post = convert_q_row(a, qtile + eg * C::kQBytes, ti, r * a.M + row0, nrows, true);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(L::qfull(sb));
         }
         ++nq;
         prev_v = v;
       }
-      if ((i & 1) != eg) continue;
-      const int j = i % kAcc;
-      if (!mbar_wait_bounded(L::afull(sb, j), (i / kAcc) & 1)) ok = false;
+      const int j = i % kUnits;
+      if (!mbar_wait_bounded(L::afull(sb, j), (i / kUnits) & 1)) ok = false;
       // the key scales this warp reads were written by the copy engine: observe
       // their arrival itself (already complete, since the MMA waited for it)
       if (KF == kFp8 && ok && !mbar_wait_bounded(L::full(sb, i % S), (i / S) & 1)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const int tbase = b * kBlock;
-      const float* ks = reinterpret_cast<const float*>(smem + L::kScaleOff + (i % S) * 2 * C::kPageScale);
       RowScore sc(post);
-      const bool whole = tbase + kBlock <= Lrow;
+      if (mine) {
+        const float* ks = reinterpret_cast<const float*>(smem + L::kScaleOff + (i % S) * 2 * C::kPageScale);
+        const uint32_t acc = trow + (uint32_t)((j * kPair + eg) * 128);
+        const bool whole = tbase + kBlock <= Lrow;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        // two 32-column loads in flight per wait
-        uint32_t raw[2][32];
-        __syncwarp();
-        tc_ld_32cols(trow + (uint32_t)(j * 128 + h * 64), raw[0]);
-        tc_ld_32cols(trow + (uint32_t)(j * 128 + h * 64 + 32), raw[1]);
-        tc_wait_ld();
+        for (int h = 0; h < 2; ++h) {
+          // two 32-column loads in flight per wait
+          uint32_t raw[2][32];
+          __syncwarp();
+          tc_ld_32cols(acc + (uint32_t)(h * 64), raw[0]);
+          tc_ld_32cols(acc + (uint32_t)(h * 64 + 32), raw[1]);
+          tc_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int c0 = h * 64 + hh * 32;
-          float x[32];
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c0 = h * 64 + hh * 32;
+            float x[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            x[k] = __uint_as_float(raw[hh][k]);
-            if (KF == kFp8) x[k] = (x[k] * qs) * ks[c0 + k];
+            for (int k = 0; k < 32; ++k) {
+              x[k] = __uint_as_float(raw[hh][k]);
+              if (KF == kFp8) x[k] = (x[k] * qs) * ks[c0 + k];
+            }
+            if (whole) sc.template add32<false>(x, tbase + c0, Lrow);
+            else sc.template add32<true>(x, tbase + c0, Lrow);
           }
-          if (whole) sc.template add32<false>(x, tbase + c0, Lrow);
-          else sc.template add32<true>(x, tbase + c0, Lrow);
         }
       }
       tc_fence_before();
