@@ -602,14 +602,21 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     clamped = __any_sync(0xffffffffu, clamped);
     if (lane == 0) {
       gpre[V] = run;
-      // long calls hand the last eighth of their blocks out at run time, which
-      // evens out the CTAs' finish times (measured: it pays from ~600 blocks per
-      // CTA; shorter calls lose more to query-tile reloads than they gain); only
-      // when a previous call left the counter at zero (its tag says so)
-      const bool dyn = *a.sched_tag == kSchedTag && run >= 600 * (int)gridDim.x;
+      // the last part of the blocks is handed out at run time, which evens out
+      // the CTAs' finish times: an eighth from ~600 blocks per CTA, a quarter
+      // from 64 (measured best on 16 x 131K bf16 / fp8 calls); NVFP4 calls
+      // below 600 stay static, since a block from another request costs a
+      // query-tile conversion there.  Only when a previous call left the
+      // counter at zero (its tag says so).
+      const int grid = (int)gridDim.x;
+      int share = 0;  // 1 / share of the blocks is dynamic
+      if (*a.sched_tag == kSchedTag) {
+        if (run >= 600 * grid) share = 8;
+        else if (KF != kNvfp4 && run >= 64 * grid) share = 4;
+      }
       ctl[0] = run;
-      ctl[1] = dyn ? run - run / 8 : run;
-      ctl[2] = dyn ? 1 : 0;
+      ctl[1] = share ? run - run / share : run;
+      ctl[2] = share ? 1 : 0;
       *cta_flags = clamped ? kErrLenClamped : 0u;
     }
   }
