@@ -316,6 +316,23 @@ IDX_API int idx_score_topk_noalloc(const void* q, const float* q_scale, int q_dt
                                    int gqa, int init_blocks, int local_blocks, int topk,
                                    int32_t* out_ids, float* out_scores, void* stream);
 
+/* idx_set_wait_limit_ns — limit (nanoseconds, process-wide) of every pipeline wait in
+ * the score kernels; 0 restores the default of 2 s.  A wait that runs past it ends
+ * its role: the CTA waits for its own copies in flight, frees its tensor memory,
+ * sets IDX_DEVERR_TIMEOUT in the workspace header and exits, so the context stays
+ * usable.  The limit is read at each call (a captured graph keeps the one of its
+ * capture).  Always returns IDX_OK. */
+IDX_API int idx_set_wait_limit_ns(uint64_t ns);
+
+/* idx_set_stall_test — diagnostic (process-wide, off by default): with on != 0, in
+ * every score CTA one role's first pipeline wait goes to a barrier that nothing
+ * completes (the 16-row kernel: warp 0, after issuing its first copies; the
+ * tensor-core kernel: the MMA issuer), so it runs out after the wait limit and the
+ * call ends through the timeout path described above, with IDX_DEVERR_TIMEOUT set.
+ * Outputs of such a call are meaningless.  Lets a test exercise failure handling
+ * on the GPU without a fault.  Always returns IDX_OK. */
+IDX_API int idx_set_stall_test(int on);
+
 /* idx_set_grid_limit — cap the number of CTAs the score kernel launches (process-
  * wide; 0 restores the default of one CTA per SM).  Results do not depend on it:
  * each block max is computed whole by one warp, so any split of the work gives the

@@ -60,6 +60,8 @@ _SIGNATURES = {
                                    _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "idx_score_local_blocks": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _I, _P, _P, _I,
                                     _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
+    "idx_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "idx_set_stall_test": (_I, [_I]),
     "idx_topk_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "idx_score_topk_noalloc": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
                                     _I, _I, _I, _I, _P, _P, _P]),
@@ -255,6 +257,16 @@ def idx_topk_merge(cand_ids, cand_scores, slot_ids, row_lens, n_slots, packed_qu
                               _dev(out_ids, "out_ids"), _dev(out_scores, "out_scores"),
                               _stream_ptr(stream))
     _check(rc, "idx_topk_merge")
+
+
+def idx_set_wait_limit_ns(ns: int) -> None:
+    """Limit of the score kernels' pipeline waits (0: the default 2 s)."""
+    _check(lib().idx_set_wait_limit_ns(int(ns)), "idx_set_wait_limit_ns")
+
+
+def idx_set_stall_test(on: bool) -> None:
+    """Diagnostic: one role per score CTA waits on a barrier nothing completes."""
+    _check(lib().idx_set_stall_test(1 if on else 0), "idx_set_stall_test")
 
 
 def idx_set_kernel_events(score_begin=None, score_end=None, topk_end=None) -> None:

@@ -291,6 +291,8 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   sa.tiles = tiles;
   sa.block_off = shard ? block_begin : 0;
   sa.shard = shard ? 1 : 0;
+  sa.wait_ns = idx::wait_limit_ns();
+  sa.stall_test = idx::stall_test();
   CUtensorMap qmap = map;
   if (wide && k_dtype != IDX_NVFP4) {
     rc = make_q_map(q_dtype, q, (int64_t)R * P * G, &qmap);
@@ -465,6 +467,16 @@ int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dtype, cons
                          page_table, n_slots, max_pages, slot_ids, row_lens, num_requests,
                          packed_queries, gqa, init_blocks, local_blocks, topk, out_ids,
                          out_scores, workspace, workspace_bytes, stream);
+}
+
+int idx_set_wait_limit_ns(uint64_t ns) {
+  idx::set_wait_limit_ns(ns);
+  return IDX_OK;
+}
+
+int idx_set_stall_test(int on) {
+  idx::set_stall_test(on);
+  return IDX_OK;
 }
 
 int idx_set_grid_limit(int max_ctas) {

@@ -55,6 +55,8 @@ struct ScoreArgs {
   int tiles;                   // wide path: 128-row tiles per request (groups = R * tiles)
   int block_off;               // global block of local block 0 (a context shard); 0 otherwise
   int shard;                   // 1: the page table holds one context shard of each request
+  unsigned long long wait_ns;  // limit of each pipeline wait before IDX_DEVERR_TIMEOUT
+  int stall_test;              // diagnostic: one role per CTA waits on a barrier nothing completes
 };
 
 struct TopkArgs {
@@ -140,6 +142,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, s
 
 // Record an error message for idx_last_error() on this host thread; returns status.
 int record_error(int status, const char* message);
+
+// Process-wide limit of the score kernels' pipeline waits (default 2 s).
+void set_wait_limit_ns(unsigned long long ns);
+unsigned long long wait_limit_ns();
+void set_stall_test(int on);
+int stall_test();
 
 // Process-wide cap on the score kernel's grid (0 = one CTA per SM).
 void set_grid_limit(int max_ctas);

@@ -66,7 +66,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_timer_ns() - t0 > limit_ns) return false;
+    // the clock is read on each of the first 64 tries (so short limits hold),
+    // then on every 64th
+    if ((it < 64u || (it & 63u) == 63u) && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

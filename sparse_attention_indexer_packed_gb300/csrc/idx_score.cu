@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   if (lane == 0) {
 #pragma unroll
     for (int d = 0; d < L::D; ++d) mbar_init(sbase + L::kBarOff + (warp * L::D + d) * 8, 1);
+    if (warp == 0) mbar_init(sbase + L::kCtlOff + 32, 1);  // the stall test's barrier
     fence_barrier_init();
   }
   if (threadIdx.x == 0) prefetch_tensormap(&payload_map);
@@ -699,7 +700,10 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       }
       cur_v = v_cur;
     }
-    if (!mbar_wait_bounded(bar, (k / D) & 1)) {
+    // stall test: warp 0's first wait goes to a barrier nothing completes
+    const bool stall = a.stall_test && warp == 0 && k == 0;
+    if (!mbar_wait_bounded(stall ? sbase + L::kCtlOff + 32 : bar, stall ? 0u : (k / D) & 1,
+                           a.wait_ns)) {
       if (lane == 0) atomicOr(cta_flags, kErrTimeout);
       aborted = true;
       break;
@@ -800,6 +804,13 @@ cudaError_t launch_bs(int key_format, const ScoreArgs& args, const CUtensorMap& 
 }
 
 }  // namespace
+
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+void set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns ? ns : 2000000000ull); }
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+std::atomic<int> g_stall_test{0};
+void set_stall_test(int on) { g_stall_test.store(on ? 1 : 0); }
+int stall_test() { return g_stall_test.load(std::memory_order_relaxed); }
 
 void set_grid_limit(int max_ctas) { g_grid_limit.store(max_ctas < 0 ? 0 : max_ctas); }
 int grid_limit() { return g_grid_limit.load(); }

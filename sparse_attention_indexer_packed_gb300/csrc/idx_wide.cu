@@ -356,6 +356,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     mbar_init(L::qfull(sb), KF == kNvfp4 ? 8 : 1);
     mbar_init(L::qempty(sb), 1);
     mbar_init(L::done(sb), 1);
+    mbar_init(sb + L::kCtlOff + 32, 1);  // the stall test's barrier
     fence_barrier_init();
     prefetch_tensormap(&kmap);
     if (KF != kNvfp4) prefetch_tensormap(&qmap);
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       if (v != prev_v) {
         if (KF != kNvfp4 && lane == 0) {
           // the previous pair's MMAs must be done with the query tiles
-          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
+          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1, a.wait_ns)) ok = false;
           if (ok) {
             const int r = v / TP;
             const int tile0 = 2 * (v - r * TP);
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         prev_v = v;
       }
       const int s = i % S;
-      if (lane == 0 && i >= S && !mbar_wait_bounded(L::empty(sb, s), ((i / S) - 1) & 1)) ok = false;
+      if (lane == 0 && i >= S && !mbar_wait_bounded(L::empty(sb, s), ((i / S) - 1) & 1, a.wait_ns)) ok = false;
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       if (lane == 0) {
@@ -515,14 +516,13 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       }
       wnext(gpre, V, v, b);
     }
-    if (!ok) {
-      if (lane == 0) {
-        atomicOr(cta_flags, kErrTimeout);
-        // let the copies still in flight land before the CTA can exit
-        for (int k = max(0, i - S); k < i; ++k)
-          (void)mbar_wait_bounded(L::full(sb, k % S), (k / S) & 1, 200000000ull);
-        if (KF != kNvfp4 && nq > 0) (void)mbar_wait_bounded(L::qfull(sb), (nq - 1) & 1, 200000000ull);
-      }
+    if (lane == 0) {
+      if (!ok) atomicOr(cta_flags, kErrTimeout);
+      // every copy this warp issued has landed before the CTA can exit, also
+      // when another role gave up early (instant when they were all consumed)
+      for (int k = max(0, i - S); k < i; ++k)
+        (void)mbar_wait_bounded(L::full(sb, k % S), (k / S) & 1, 200000000ull);
+      if (KF != kNvfp4 && nq > 0) (void)mbar_wait_bounded(L::qfull(sb), (nq - 1) & 1, 200000000ull);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -533,7 +533,13 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       if (u0 < u1) wlocate(gpre, V, u0, v, b);
       for (int u = u0; u < u1; ++u, ++i) {
         if (v != prev_v) {
-          if (!mbar_wait_bounded(L::qfull(sb), nq & 1)) { ok = false; break; }
+          // stall test: the first wait goes to a barrier nothing completes
+          const bool stall = a.stall_test && nq == 0;
+          if (!mbar_wait_bounded(stall ? sb + L::kCtlOff + 32 : L::qfull(sb), stall ? 0u : nq & 1,
+                                 a.wait_ns)) {
+            ok = false;
+            break;
+          }
           ++nq;
           prev_v = v;
           nt = min(kPair, a.tiles - 2 * (v % TP));
@@ -542,14 +548,14 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         uint32_t opnd;
         if constexpr (KF == kNvfp4) {
           const int d = i % SD;
-          if (!mbar_wait_bounded(L::dfull(sb, d), (i / SD) & 1)) { ok = false; break; }
+          if (!mbar_wait_bounded(L::dfull(sb, d), (i / SD) & 1, a.wait_ns)) { ok = false; break; }
           opnd = sb + L::kDecOff + d * 32768;
         } else {
-          if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1)) { ok = false; break; }
+          if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1, a.wait_ns)) { ok = false; break; }
           opnd = sb + L::kStageOff + s * C::kStageBytes;
         }
         const int j = i % kUnits;
-        if (i >= kUnits && !mbar_wait_bounded(L::aempty(sb, j), ((i / kUnits) - 1) & 1)) { ok = false; break; }
+        if (i >= kUnits && !mbar_wait_bounded(L::aempty(sb, j), ((i / kUnits) - 1) & 1, a.wait_ns)) { ok = false; break; }
         tc_fence_after();
         // both tiles of the pair against the same staged keys
         for (int t = 0; t < nt; ++t) {
@@ -615,7 +621,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         if (KF == kNvfp4) {
           // each group writes its own f16 query tile once every MMA of the
           // previous pair has completed
-          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1)) ok = false;
+          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1, a.wait_ns)) ok = false;
           if (!__all_sync(0xffffffffu, ok)) break;
           if (mine) post = convert_q_row(a, qtile + eg * C::kQBytes, ti, r * a.M + row0, nrows, true);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -626,10 +632,10 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         prev_v = v;
       }
       const int j = i % kUnits;
-      if (!mbar_wait_bounded(L::afull(sb, j), (i / kUnits) & 1)) ok = false;
+      if (!mbar_wait_bounded(L::afull(sb, j), (i / kUnits) & 1, a.wait_ns)) ok = false;
       // the key scales this warp reads were written by the copy engine: observe
       // their arrival itself (already complete, since the MMA waited for it)
-      if (KF == kFp8 && ok && !mbar_wait_bounded(L::full(sb, i % S), (i / S) & 1)) ok = false;
+      if (KF == kFp8 && ok && !mbar_wait_bounded(L::full(sb, i % S), (i / S) & 1, a.wait_ns)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const int tbase = b * kBlock;
@@ -676,8 +682,8 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     int i = 0;
     for (int u = u0; u < u1; ++u, ++i) {
       const int s = i % S, d = i % SD;
-      if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1)) ok = false;
-      if (ok && i >= SD && !mbar_wait_bounded(L::dempty(sb, d), ((i / SD) - 1) & 1)) ok = false;
+      if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1, a.wait_ns)) ok = false;
+      if (ok && i >= SD && !mbar_wait_bounded(L::dempty(sb, d), ((i / SD) - 1) & 1, a.wait_ns)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       decode_token(sb + L::kStageOff + s * C::kStageBytes, sb + L::kScaleOff + s * 2 * C::kPageScale,
                    sb + L::kDecOff + d * 32768, n);

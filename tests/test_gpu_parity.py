@@ -333,3 +333,31 @@ def test_topk_warp_rows_match_cta_rows():
     assert np.array_equal(warp.scores.view(np.uint32), cta.scores.view(np.uint32))
     ref = oracle.index.index_step(**oracle_kwargs(b))
     _check_all_rows(b, warp, ref)
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype,P,G", [("bf16", "bf16", 4, 4), ("bf16", "bf16", 40, 4),
+                                                 ("nvfp4", "bf16", 40, 4)])
+def test_wait_timeout_is_reported_and_the_context_survives(k_dtype, q_dtype, P, G):
+    """A wait that nothing completes (the stall test: one role per score CTA
+    waits on a barrier no one arrives at, with a 20 ms limit) must end the call
+    through the timeout path -- copies in flight waited for, TMEM freed,
+    IDX_DEVERR_TIMEOUT in the workspace -- instead of hanging or faulting, and
+    the next call must be exact again.  P x G = 40 x 4 takes the tensor-core
+    path, whose other roles then also run out of their waits."""
+    import sparse_attention_indexer_packed_gb300 as idx
+    spec = workloads.small_spec("to", 701, k_dtype, q_dtype, R=4, P=P, G=G,
+                                len_range=(2000, 9000), topk=16)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    try:
+        idx.idx_set_wait_limit_ns(20_000_000)
+        idx.idx_set_stall_test(True)
+        bad = _gpu.run(b, planes=planes)
+    finally:
+        idx.idx_set_stall_test(False)
+        idx.idx_set_wait_limit_ns(0)
+    assert bad.flags & 2, f"expected IDX_DEVERR_TIMEOUT, flags {bad.flags:#x}"
+    good = _gpu.run(b, planes=planes)
+    assert good.flags == 0
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_all_rows(b, good, ref)
