@@ -94,7 +94,7 @@ struct Shared {
   uint32_t digit, need, bin;
 };
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, 8) topk_kernel(const TopkArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   unsigned long long* sel = sh.sel;
@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 // bin: when that bin is taken whole they stop; otherwise they end at the exact
 // c-th largest key T, keys above T are taken, and of the keys equal to T the
 // lowest ids, counted with ballots in id order.  The chosen entries are
-// compacted in id order and each is placed by its rank (key desc, id asc).
+// compacted in id order and ordered by (key desc, id asc): up to 64 of them by
+// a bitonic sort in registers, more by each one's rank among them.
 // Same selection, outputs and score recovery as topk_kernel.
 // ---------------------------------------------------------------------------
 // Four rows per CTA and one 2 KB slot per warp (histogram while the threshold
@@ -318,7 +319,7 @@ union WarpSlot {
 };
 
 template <int R>
-__global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(32 * kRowsPerCta, 12) topk_warp_kernel(const TopkArgs a) {
   __shared__ WarpSlot sh[kRowsPerCta];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -466,6 +467,46 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkA
     n += __popc(m);
   }
   __syncwarp();
+  if (n <= 64) {
+    // up to 64 entries: a descending bitonic sort of the (key, id) composites,
+    // two per lane (element e = lane + 32 h); unused slots hold 0, below any entry
+    unsigned long long x[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) x[h] = lane + 32 * h < n ? list[lane + 32 * h] : 0ull;
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        if (j == 32) {
+          // partners in the same lane: e (h = 0) below e + 32 (h = 1), and
+          // (e & k) == 0 for k = 64, so the larger goes to h = 0
+          const unsigned long long lo = x[0] > x[1] ? x[0] : x[1];
+          const unsigned long long hi = x[0] > x[1] ? x[1] : x[0];
+          x[0] = lo;
+          x[1] = hi;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = lane + 32 * h;
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[h], j);
+            const bool lower = (e & j) == 0;   // e is the lower index of the pair
+            const bool desc = (e & k) == 0;    // this run sorts descending
+            const bool take_max = lower == desc;
+            x[h] = take_max ? (x[h] > y ? x[h] : y) : (x[h] > y ? y : x[h]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = lane + 32 * h;
+      if (e < n) {
+        out_ids[nf + e] = 0x7fffffff - (int)(uint32_t)(x[h] & 0xffffffffull);
+        out_sc[nf + e] = key_value((uint32_t)(x[h] >> 32));
+      }
+    }
+    return;
+  }
   for (int j = lane; j < n; j += 32) {
     const unsigned long long x = list[j];
     int rank = 0;

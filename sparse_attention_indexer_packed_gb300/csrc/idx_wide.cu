@@ -644,17 +644,21 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         const float* ks = reinterpret_cast<const float*>(smem + L::kScaleOff + (i % S) * 2 * C::kPageScale);
         const uint32_t acc = trow + (uint32_t)((j * kPair + eg) * 128);
         const bool whole = tbase + kBlock <= Lrow;
+        // kLd 32-column loads in flight per wait: for bf16 all four of the
+        // block's (one TMEM round trip); two for e4m3, whose per-column key
+        // scales need the registers (measured slower with four), and for
+        // NVFP4, whose decoder warps leave fewer registers per thread
+        constexpr int kLd = KF == kBf16 ? 4 : 2;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          // two 32-column loads in flight per wait
-          uint32_t raw[2][32];
+        for (int h = 0; h < 4 / kLd; ++h) {
+          uint32_t raw[kLd][32];
           __syncwarp();
-          tc_ld_32cols(acc + (uint32_t)(h * 64), raw[0]);
-          tc_ld_32cols(acc + (uint32_t)(h * 64 + 32), raw[1]);
+#pragma unroll
+          for (int hh = 0; hh < kLd; ++hh) tc_ld_32cols(acc + (uint32_t)((h * kLd + hh) * 32), raw[hh]);
           tc_wait_ld();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int c0 = h * 64 + hh * 32;
+          for (int hh = 0; hh < kLd; ++hh) {
+            const int c0 = (h * kLd + hh) * 32;
             float x[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) {

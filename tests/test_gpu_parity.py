@@ -313,14 +313,17 @@ def test_batch_invariance_of_a_request():
     assert np.array_equal(a.scores[0].view(np.uint32), o.scores[0].view(np.uint32))
 
 
-def test_topk_warp_rows_match_cta_rows():
+@pytest.mark.parametrize("topk,max_len", [(16, 9000), (100, 20000)])
+def test_topk_warp_rows_match_cta_rows(topk, max_len):
     """Many rows of at most 256 blocks (here 4 prefill-like requests of 256
     query tokens x 4 heads: 4096 rows) take the warp-per-row top-k; the same
     rows behind a page table wider than 512 pages take the CTA-per-row one.
     Both must give the oracle's selection and agree bit for bit, including rows
-    whose scores are all equal (zero queries: every tie goes to the lower id)."""
+    whose scores are all equal (zero queries: every tie goes to the lower id).
+    A budget of 16 blocks orders its chosen entries by the in-register sort
+    (at most 64), one of 100 over rows of up to 157 blocks by the rank count."""
     spec = workloads.small_spec("tk", 501, "bf16", "bf16", R=4, P=256, G=4,
-                                len_range=(300, 9000), topk=16)
+                                len_range=(300, max_len), topk=topk)
     b = workloads.make_batch(spec)
     b.q[1] = 0                      # request 1: every block score 0
     b.q[2, 7, 1] = 0                # one row of request 2
@@ -336,6 +339,7 @@ def test_topk_warp_rows_match_cta_rows():
 
 
 @pytest.mark.parametrize("k_dtype,q_dtype,P,G", [("bf16", "bf16", 4, 4), ("bf16", "bf16", 40, 4),
+                                                 ("fp8_e4m3", "fp8_e4m3", 8, 8),
                                                  ("nvfp4", "bf16", 40, 4)])
 def test_wait_timeout_is_reported_and_the_context_survives(k_dtype, q_dtype, P, G):
     """A wait that nothing completes (the stall test: one role per score CTA
