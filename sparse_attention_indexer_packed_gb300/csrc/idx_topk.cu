@@ -15,7 +15,9 @@
 // the bits every candidate shares, one shared 256-bin histogram per digit)
 // narrow them to the keys at or above the threshold's bin, usually after one
 // pass.  Each remaining (key, id) entry is then placed by its rank among them,
-// ties going to the lower id; entries ranked c or later are dropped.  The score
+// ties going to the lower id; entries ranked c or later are dropped.  (One
+// warp sorting them with a bitonic network measured slower here, also with
+// 1024 rows in flight: its chain is longer than n threads' rank counts.)  The score
 // written out is recovered from the key, so nothing is read back from memory.
 #include <cuda_runtime.h>
 #include <math.h>
@@ -30,7 +32,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxWorld = 8;  // context shards a merge accepts
 constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = 16;  // independent loads in flight per thread
+constexpr int kBatch = 16;  // independent loads in flight per thread (long rows)
 // The exact step ranks at most kCap entries (kCap >= the largest topk).
 constexpr int kCap = 1024;
 static_assert(kCap >= kMaxTopk, "the exact step must hold a whole selection");
@@ -85,6 +87,87 @@ __device__ __forceinline__ RowPlan row_plan(const TopkArgs& a, int r, int i) {
   return p;
 }
 
+// Keys of candidates [0, ncand) (block maxima bm[0..)) into keys[], with B
+// loads in flight per thread; returns this thread's smallest and largest key.
+template <int B>
+__device__ __forceinline__ void load_keys(const float* bm, int ncand, uint32_t* keys, int tid,
+                                          uint32_t& kmin, uint32_t& kmax) {
+  for (int t0 = 0; t0 < ncand; t0 += kThreads * B) {
+    float v[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int t = t0 + u * kThreads + tid;
+      v[u] = t < ncand ? bm[t] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int t = t0 + u * kThreads + tid;
+      if (t < ncand) {
+        const uint32_t k = order_key(v[u]);
+        keys[t] = k;
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
+    }
+  }
+}
+
+// Descending bitonic sort of 32 E 64-bit values held by one warp, element
+// e = lane + 32 h in x[h] (E a power of two).  Partners closer than 32 are
+// exchanged by shuffles, farther ones inside the lane's registers.
+template <int E>
+__device__ __forceinline__ void warp_sort_desc(unsigned long long (&x)[E], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 32) {
+        const int hj = j >> 5;
+#pragma unroll
+        for (int h = 0; h < E; ++h) {
+          if ((h & hj) == 0) {
+            // pair (e, e + j), e = lane + 32 h; (e & k) depends on h alone
+            const bool desc = ((32 * h) & k) == 0;
+            const unsigned long long a = x[h], b = x[h | hj];
+            const bool swap = desc ? a < b : a > b;
+            x[h] = swap ? b : a;
+            x[h | hj] = swap ? a : b;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < E; ++h) {
+          const int e = lane + 32 * h;
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[h], j);
+          // the lower index of a descending run keeps the larger value
+          const bool take_max = ((e & j) == 0) == ((e & k) == 0);
+          x[h] = take_max ? (x[h] > y ? x[h] : y) : (x[h] > y ? y : x[h]);
+        }
+      }
+    }
+  }
+}
+
+// Sorts list[0, n) (n <= 32 E) in one warp and writes entries of rank < c to
+// the outputs at nf + rank.  Unused slots hold 0, below every (key, id) entry.
+template <int E>
+__device__ __forceinline__ void warp_place_sorted(const unsigned long long* list, int n, int c,
+                                                  int nf, int lane, int32_t* out_ids,
+                                                  float* out_sc) {
+  unsigned long long x[E];
+#pragma unroll
+  for (int h = 0; h < E; ++h) x[h] = lane + 32 * h < n ? list[lane + 32 * h] : 0ull;
+  warp_sort_desc<E>(x, lane);
+#pragma unroll
+  for (int h = 0; h < E; ++h) {
+    const int e = lane + 32 * h;
+    if (e < n && e < c) {
+      out_ids[nf + e] = 0x7fffffff - (int)(uint32_t)(x[h] & 0xffffffffull);
+      out_sc[nf + e] = key_value((uint32_t)(x[h] >> 32));
+    }
+  }
+}
+
 struct Shared {
   uint32_t hist[256];
   unsigned long long sel[kCap];
@@ -94,7 +177,12 @@ struct Shared {
   uint32_t digit, need, bin;
 };
 
-__global__ void __launch_bounds__(kThreads, 8) topk_kernel(const TopkArgs a) {
+// kMinCtas = 8 caps registers at 32 so that eight rows share an SM (more than
+// six rows per SM: one wave instead of two); 0 (no minimum) leaves the
+// compiler the registers that keep a long row's loads in flight, measured
+// faster for a few hundred rows of ~1000 blocks.
+template <int kMinCtas>
+__global__ void __launch_bounds__(kThreads, kMinCtas) topk_kernel(const TopkArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
   unsigned long long* sel = sh.sel;
@@ -139,24 +227,11 @@ __global__ void __launch_bounds__(kThreads, 8) topk_kernel(const TopkArgs a) {
 
   // ---- candidate keys ----------------------------------------------------
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int t0 = 0; t0 < ncand; t0 += kThreads * kBatch) {
-    float v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int t = t0 + u * kThreads + tid;
-      v[u] = t < ncand ? bmg[fi + t] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int t = t0 + u * kThreads + tid;
-      if (t < ncand) {
-        const uint32_t k = order_key(v[u]);
-        keys[t] = k;
-        kmin = min(kmin, k);
-        kmax = max(kmax, k);
-      }
-    }
-  }
+  // as many loads in flight as the row needs, up to kBatch (predicated-off
+  // loads still cost issue slots)
+  if (ncand <= kThreads) load_keys<1>(bmg + fi, ncand, keys, tid, kmin, kmax);
+  else if (ncand <= 4 * kThreads) load_keys<4>(bmg + fi, ncand, keys, tid, kmin, kmax);
+  else load_keys<kBatch>(bmg + fi, ncand, keys, tid, kmin, kmax);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
@@ -319,7 +394,7 @@ union WarpSlot {
 };
 
 template <int R>
-__global__ void __launch_bounds__(32 * kRowsPerCta, 12) topk_warp_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkArgs a) {
   __shared__ WarpSlot sh[kRowsPerCta];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -468,43 +543,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta, 12) topk_warp_kernel(const T
   }
   __syncwarp();
   if (n <= 64) {
-    // up to 64 entries: a descending bitonic sort of the (key, id) composites,
-    // two per lane (element e = lane + 32 h); unused slots hold 0, below any entry
-    unsigned long long x[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) x[h] = lane + 32 * h < n ? list[lane + 32 * h] : 0ull;
-#pragma unroll
-    for (int k = 2; k <= 64; k <<= 1) {
-#pragma unroll
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        if (j == 32) {
-          // partners in the same lane: e (h = 0) below e + 32 (h = 1), and
-          // (e & k) == 0 for k = 64, so the larger goes to h = 0
-          const unsigned long long lo = x[0] > x[1] ? x[0] : x[1];
-          const unsigned long long hi = x[0] > x[1] ? x[1] : x[0];
-          x[0] = lo;
-          x[1] = hi;
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = lane + 32 * h;
-            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[h], j);
-            const bool lower = (e & j) == 0;   // e is the lower index of the pair
-            const bool desc = (e & k) == 0;    // this run sorts descending
-            const bool take_max = lower == desc;
-            x[h] = take_max ? (x[h] > y ? x[h] : y) : (x[h] > y ? y : x[h]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = lane + 32 * h;
-      if (e < n) {
-        out_ids[nf + e] = 0x7fffffff - (int)(uint32_t)(x[h] & 0xffffffffull);
-        out_sc[nf + e] = key_value((uint32_t)(x[h] >> 32));
-      }
-    }
+    warp_place_sorted<2>(list, n, n, nf, lane, out_ids, out_sc);
     return;
   }
   for (int j = lane; j < n; j += 32) {
@@ -627,17 +666,8 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerCta) merge_kernel(const Merg
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
-  const int rows = a.R * a.M;
-  if (rows == 0) return cudaSuccess;
-  // many short rows: a warp per row (measured: below about 16 rows per SM the
-  // CTA-per-row kernel's shorter per-row latency wins)
-  int cur = 0;
-  if (cudaGetDevice(&cur) == cudaSuccess && rows >= 16 * cached_sm_count(cur)) {
-    if (a.nb_cap <= 64) return launch_topk_warp<2>(a, rows, stream);
-    if (a.nb_cap <= 128) return launch_topk_warp<4>(a, rows, stream);
-    if (a.nb_cap <= 256) return launch_topk_warp<8>(a, rows, stream);
-  }
+template <int kMinCtas>
+cudaError_t launch_topk_cta(const TopkArgs& a, int rows, cudaStream_t stream) {
   const size_t smem = sizeof(Shared) + (size_t)a.nb_cap * sizeof(uint32_t);
   // the limit is raised once per device to what the largest page table
   // (65536 pages: 32768 blocks) can need; each launch asks for its own size
@@ -645,8 +675,8 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = smem_limit_once(topk_kernel, (int)(sizeof(Shared) + 32768 * sizeof(uint32_t)), dev,
-                      attr_done);
+  e = smem_limit_once(topk_kernel<kMinCtas>, (int)(sizeof(Shared) + 32768 * sizeof(uint32_t)),
+                      dev, attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)rows);
@@ -658,9 +688,23 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_kernel, a);
+  e = cudaLaunchKernelEx(&cfg, topk_kernel<kMinCtas>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
+  const int rows = a.R * a.M;
+  if (rows == 0) return cudaSuccess;
+  // many short rows: a warp per row (measured: below about 16 rows per SM the
+  // CTA-per-row kernel's shorter per-row latency wins)
+  int cur = 0;
+  if (cudaGetDevice(&cur) == cudaSuccess && rows >= 16 * cached_sm_count(cur)) {
+    if (a.nb_cap <= 64) return launch_topk_warp<2>(a, rows, stream);
+    if (a.nb_cap <= 128) return launch_topk_warp<4>(a, rows, stream);
+    if (a.nb_cap <= 256) return launch_topk_warp<8>(a, rows, stream);
+  }
+  if (rows > 6 * cached_sm_count(cur)) return launch_topk_cta<8>(a, rows, stream);
+  return launch_topk_cta<0>(a, rows, stream);
 }
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {

@@ -233,6 +233,20 @@ def test_zero_requests():
     torch.cuda.synchronize()
 
 
+def test_most_requests_per_call():
+    """IDX_MAX_REQUESTS (2048) requests of 16 packed rows in one call, short
+    ragged contexts and a few pad requests: 32768 rows, so the warp-per-row
+    top-k takes them."""
+    spec = workloads.small_spec("mr", 504, "bf16", "bf16", R=2048, len_range=(1, 1200),
+                                pad_requests=(0, 777, 2047), topk=12)
+    b = workloads.make_batch(spec)
+    out = _gpu.run(b)
+    assert out.flags == 0
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_blockmax(b, out, ref)
+    _check_all_rows(b, out, ref)
+
+
 def test_topk_edge_values():
     """topk = init + local (no free choice), topk = 256, all scores equal."""
     spec = workloads.small_spec("e", 503, "bf16", "bf16", R=3, len_range=(1, 40000), topk=6)

@@ -93,3 +93,12 @@ def test_wide_results_do_not_depend_on_the_grid(k_dtype, q_dtype):
             assert np.array_equal(part.scores.view(np.uint32), full.scores.view(np.uint32))
     finally:
         idx.idx_set_grid_limit(0)
+
+
+def test_most_rows_per_request():
+    """IDX_MAX_ROWS_PER_REQUEST (32768) rows in one request: 4096 query tokens
+    x 8 heads, 256 tiles in 128 pairs, rows from ~100 to 5000 tokens."""
+    b = workloads.make_batch(_spec("bf16", "bf16", 431, 1, 4096, 8, (4200, 5000), (), 1, 4, 24))
+    out = _gpu.run(b)
+    assert out.flags == 0
+    _check(b, out, oracle.index.index_step(**oracle_kwargs(b)))
