@@ -176,6 +176,38 @@ __device__ __forceinline__ int wpage(const ScoreArgs& a, const int* gpre, const 
   return p;
 }
 
+// Step (1) of the group table: gpre[v] = the longest draft row (clamped to the
+// page table) among those with a row in group v, by atomicMax over all threads,
+// B rows per thread per round with their loads in flight together.  Returns
+// whether this thread saw a live request's row clamped (CTA 0 only).
+template <int B>
+__device__ __forceinline__ bool group_extents(const ScoreArgs& a, int* gpre, int TP, int RP) {
+  bool clamped = false;
+  const int cap = a.max_pages * kPage;
+  for (int x0 = 0; x0 < RP; x0 += B * (int)blockDim.x) {
+    int len[B];
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      const int x = x0 + e * (int)blockDim.x + (int)threadIdx.x;
+      len[e] = x < RP ? __ldg(a.row_lens + x) : 0;
+    }
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      const int x = x0 + e * (int)blockDim.x + (int)threadIdx.x;
+      const int L = len[e];
+      if (L <= 0) continue;
+      const int r = x / a.P, j = x - r * a.P;
+      const int t0 = (j * a.G) / kWRows, t1 = (j * a.G + a.G - 1) / kWRows;
+      for (int t = t0 / 2; t <= t1 / 2; ++t) atomicMax(&gpre[r * TP + t], min(L, cap));
+      if (blockIdx.x == 0 && L > cap) {
+        const int slot = __ldg(a.slot_ids + r);
+        clamped |= slot >= 0 && slot < a.n_slots;
+      }
+    }
+  }
+  return clamped;
+}
+
 // Per-thread row scores over one block, fed 32 columns at a time.
 struct RowMax {
   float m = -INFINITY;
@@ -375,28 +407,20 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
   // group v = (request v / TP, tiles 2 (v % TP) and 2 (v % TP) + 1): TP pairs
   // per request, the last a single tile when a request has an odd count
   // (1) every thread takes draft rows: a tile's extent is the longest of the
-  // draft rows any of its rows belongs to (one load per draft row, all in flight
-  // at once); (2) warp 0 turns extents into block counts and prefix sums.
+  // draft rows any of its rows belongs to; (2) warp 0 turns extents into block
+  // counts and prefix sums.
   const int TP = (a.tiles + 1) / 2;
   const int V = a.R * TP;
   for (int v = threadIdx.x; v < V; v += blockDim.x) gpre[v] = 0;
   if (threadIdx.x == 0) *cta_flags = 0u;
   __syncthreads();
   {
-    bool clamped = false;
     const int RP = a.R * a.P;
-    const int cap = a.max_pages * kPage;
-    for (int x = threadIdx.x; x < RP; x += blockDim.x) {
-      const int L = __ldg(a.row_lens + x);
-      if (L <= 0) continue;
-      const int r = x / a.P, j = x - r * a.P;
-      const int t0 = (j * a.G) / kWRows, t1 = (j * a.G + a.G - 1) / kWRows;
-      for (int t = t0 / 2; t <= t1 / 2; ++t) atomicMax(&gpre[r * TP + t], min(L, cap));
-      if (blockIdx.x == 0 && L > cap) {
-        const int slot = __ldg(a.slot_ids + r);
-        clamped |= slot >= 0 && slot < a.n_slots;
-      }
-    }
+    // a prefill chunk has thousands of draft rows: eight loads in flight per
+    // thread (one round trip instead of one per row); a verify pack's few
+    // rows take one each (the batched loop measured slower there)
+    const bool clamped = RP > (int)blockDim.x ? group_extents<8>(a, gpre, TP, RP)
+                                              : group_extents<1>(a, gpre, TP, RP);
     if (clamped) atomicOr(cta_flags, kErrLenClamped);
   }
   __syncthreads();

@@ -265,13 +265,24 @@ def test_topk_edge_values():
     assert np.array_equal(out.ids, ref.ids)
 
 
-def test_bad_page_ids_are_flagged_not_read():
-    spec = workloads.small_spec("bp", 504, "fp8_e4m3", "fp8_e4m3", R=2, len_range=(3000, 4000))
+@pytest.mark.parametrize("P,G,grid", [(4, 4, 0), (40, 4, 0), (40, 4, 1)])
+def test_bad_page_ids_are_flagged_not_read(P, G, grid):
+    """Page ids outside the pool are flagged and not read, on the 16-row path
+    and on the tensor-core path; with one CTA the late bad page sits in a later
+    batch of the producer's page lookups than the first."""
+    import sparse_attention_indexer_packed_gb300 as idx
+    spec = workloads.small_spec("bp", 504, "fp8_e4m3", "fp8_e4m3", R=2, P=P, G=G,
+                                len_range=(3000, 4000))
     b = workloads.make_batch(spec)
     pt = b.page_table.clone()
     pt[int(b.slot_ids[0]), 3] = b.num_pages + 5
     pt[int(b.slot_ids[1]), 0] = -7
-    out = _gpu.run(b, page_table=pt)
+    pt[int(b.slot_ids[1]), 45] = b.num_pages
+    try:
+        idx.idx_set_grid_limit(grid)
+        out = _gpu.run(b, page_table=pt)
+    finally:
+        idx.idx_set_grid_limit(0)
     assert out.flags & 1
 
 
