@@ -572,6 +572,8 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   // ---- group table: block prefix sums and slots of every group -------------
   const int V = a.perrow ? a.R * a.P : a.R;
   if (warp == 0) {
+    // read up front, so its round trip overlaps the row-length loads
+    const bool tag_ok = lane == 0 && *a.sched_tag == kSchedTag;
     int run = 0;
     bool clamped = false;
     for (int v0 = 0; v0 < V; v0 += 32) {
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       // counter at zero (its tag says so).
       const int grid = (int)gridDim.x;
       int share = 0;  // 1 / share of the blocks is dynamic
-      if (*a.sched_tag == kSchedTag) {
+      if (tag_ok) {
         if (run >= 600 * grid) share = 8;
         else if (KF != kNvfp4 && run >= 64 * grid) share = 4;
       }
@@ -619,6 +621,20 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       ctl[1] = share ? run - run / share : run;
       ctl[2] = share ? 1 : 0;
       *cta_flags = clamped ? kErrLenClamped : 0u;
+    }
+  } else {
+    // meanwhile the other warps of the grid bring every request's page-table
+    // row into L2 (one 128-byte line per thread), so each warp's first page
+    // lookup after the table is an L2 hit rather than a DRAM (and TLB) miss;
+    // skipped when the table is wider than the grid's threads
+    const int lines_per = (a.max_pages + 31) / 32;
+    const int nthr = (int)gridDim.x * (NC - 1) * 32;
+    const int gt = ((int)blockIdx.x * (NC - 1) + warp - 1) * 32 + lane;
+    if (a.R * lines_per <= nthr && gt < a.R * lines_per) {
+      const int r = gt / lines_per, line = gt - r * lines_per;
+      const int slot = __ldg(a.slot_ids + r);
+      if (slot >= 0 && slot < a.n_slots)
+        prefetch_l2(a.page_table + (size_t)slot * a.max_pages + (size_t)line * 32);
     }
   }
   __syncthreads();
@@ -631,13 +647,16 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   int sk = (int)((long long)Us * blockIdx.x / gridDim.x) + warp;  // next static unit
 
   // this warp's units: its share of the CTA's static range, then blocks taken
-  // one at a time from the dynamic pool (the take is issued one unit ahead)
+  // one at a time from the dynamic pool (each take is issued one unit ahead:
+  // the first when the last static unit is handed out, not at the start, where
+  // its round trip would delay the first copies)
   int ahead = -1;
-  if (dyn && lane == 0) ahead = Us + (int)atomicAdd(a.sched_counter, 1u);
+  if (dyn && sk >= s1 && lane == 0) ahead = Us + (int)atomicAdd(a.sched_counter, 1u);
   auto next_unit = [&]() -> int {
     if (sk < s1) {
       const int u = sk;
       sk += NC;
+      if (dyn && sk >= s1 && lane == 0) ahead = Us + (int)atomicAdd(a.sched_counter, 1u);
       return u;
     }
     if (!dyn) return -1;
