@@ -72,11 +72,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
-// A hint to bring the 128-byte line holding p into L2 (no result, nothing waits).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------

@@ -110,6 +110,11 @@ __device__ __forceinline__ int token_cap(const ScoreArgs& a) {
   return (2 * a.block_off + a.max_pages) * kPage;
 }
 
+// A hint to bring the 128-byte line holding p into L2 (no result, nothing waits).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Geometry of scoring group v (a request when packed, a draft row when per-row).
 __device__ Group group_info(const ScoreArgs& a, int v) {
   Group g;
