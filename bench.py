@@ -17,6 +17,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -552,17 +553,17 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
             d_in[i].copy_(h_in, non_blocking=True)
             ev_in[i].record(cs)
 
-    def compute(k):
+    def compute(k, st):
         i = k % 2
-        stream.wait_event(ev_in[i])
+        st.wait_event(ev_in[i])
         if k >= 2:
-            stream.wait_event(ev_out[i])       # step k - 2's outputs are out
+            st.wait_event(ev_out[i])           # step k - 2's outputs are out
         q, pt, sl, ln = vin[i][:4]
         qs = vin[i][4] if batch.q_scale is not None else None
         kp, ks = pools[k % npool]
         fn(q, qs, kp, ks, s.k_dtype, pt, sl, ln, s.packed_queries, s.gqa,
-           s.init_blocks, s.local_blocks, topk, vout[i][0], vout[i][1], wsp, stream)
-        ev_used[i].record(stream)
+           s.init_blocks, s.local_blocks, topk, vout[i][0], vout[i][1], wsp, st)
+        ev_used[i].record(st)
 
     def copy_out(k):
         i = k % 2
@@ -571,28 +572,49 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
             h_out[i].copy_(d_out[i], non_blocking=True)
             ev_out[i].record(cs)
 
-    def run(n, t0=None, t1=None):
+    def run(n):
+        # on the current stream (the caller's, or a graph's capture stream)
+        st = torch.cuda.current_stream(dev)
         start = torch.cuda.Event()
-        if t0 is not None:
-            t0.record(stream)
-        start.record(stream)
+        start.record(st)
         cs.wait_event(start)
         copy_in(0)
         for k in range(n):
             if k + 1 < n:
                 copy_in(k + 1)
-            compute(k)
+            compute(k, st)
             copy_out(k)
-        stream.wait_event(ev_out[(n - 1) % 2])
-        if t1 is not None:
-            t1.record(stream)
+        st.wait_event(ev_out[(n - 1) % 2])
 
     run(max(3, args.warmup))
     torch.cuda.synchronize(dev)
-    n = max(10, min(args.steps, 200))
+    # a serving loop replays the captured steps: G steps (a multiple of the
+    # buffer sets and of the pool copies) per graph
+    G = 2 * npool // math.gcd(2, npool)
+    while G < 64:
+        G *= 2
+    reps = max(2, -(-max(10, min(args.steps, 200)) // G))
+    n = reps * G
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    run(n, t0, t1)
+    mode = "graph"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run(G)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t1.record(stream)
+    except RuntimeError as e:   # capture refused: time the same pipeline eagerly
+        torch.cuda.synchronize(dev)
+        mode = "eager (graph capture failed: %s)" % str(e).splitlines()[0][:100]
+        t0.record(stream)
+        for _ in range(reps):
+            run(G)
+        t1.record(stream)
     torch.cuda.synchronize(dev)
     us = t0.elapsed_time(t1) * 1e3 / n
     # the staged buffers must give what the same call on separate device tensors gives
@@ -602,7 +624,7 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
        s.k_dtype, batch.page_table.to(dev), batch.slot_ids.to(dev), batch.row_lens.to(dev),
        s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, topk, ref_ids, ref_sc, wsp, stream)
     torch.cuda.synchronize(dev)
-    got = _views(h_out[(n - 1) % 2], outs, ooffs)
+    got = _views(h_out[(G - 1) % 2], outs, ooffs)
     if not (torch.equal(got[0], ref_ids.cpu()) and
             torch.equal(got[1].view(torch.int32), ref_sc.cpu().view(torch.int32))):
         raise RuntimeError("staged end-to-end outputs differ from the device-resident call")
@@ -611,7 +633,9 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
             "note": "keys stay resident in the pool (a layer's index-K cache); q, page table, "
                     "slot ids and row lengths are copied in (one pinned staging buffer, one "
                     "copy), ids and scores copied out (one copy), on a copy stream that "
-                    "overlaps them with the neighbouring steps' kernels"}
+                    "overlaps them with the neighbouring steps' kernels; the steps replayed "
+                    "from a CUDA graph of steps_per_graph steps",
+            "steps_per_graph": G, "mode": mode}
 
 
 def _oracle_sample(batch, budget_s: float, block_score: str = "max"):
