@@ -75,13 +75,16 @@ def test_wide_lse_parity(k_dtype, q_dtype):
     _check(b, out, oracle.index.index_step(**oracle_kwargs(b), block_score="lse"))
 
 
+@pytest.mark.parametrize("P,G", [(40, 4), (8, 8)])
 @pytest.mark.parametrize("k_dtype,q_dtype", [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3"),
                                              ("nvfp4", "bf16")])
-def test_wide_results_do_not_depend_on_the_grid(k_dtype, q_dtype):
+def test_wide_results_do_not_depend_on_the_grid(k_dtype, q_dtype, P, G):
     """With 1, 3 and 7 CTAs every CTA walks through many tiles (query-tile
-    reloads, accumulator ring wrap-arounds); the scores are bit-identical to the
-    full grid's, because each block's sums do not depend on who computes them."""
-    b = workloads.make_batch(_spec(k_dtype, q_dtype, 421, 3, 40, 4, (1, 4000), (), 1, 2, 16))
+    reloads, key-stage and accumulator ring wrap-arounds); the scores are
+    bit-identical to the full grid's, because each block's sums do not depend on
+    who computes them.  P x G = 64 is one tile per request (each group a lone
+    tile)."""
+    b = workloads.make_batch(_spec(k_dtype, q_dtype, 421, 3, P, G, (1, 4000), (), 1, 2, 16))
     planes = _gpu.device_planes(b)
     full = _gpu.run(b, planes=planes)
     try:
