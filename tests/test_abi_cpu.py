@@ -111,3 +111,60 @@ def test_cpu_tensors_are_refused():
         idx.idx_store_nvfp4(torch.zeros((1, 128), dtype=torch.bfloat16),
                             torch.zeros(1, dtype=torch.int64),
                             (torch.zeros((64, 64), dtype=torch.uint8), torch.zeros((64, 8), dtype=torch.uint8)))
+
+
+def _shard(L, **over):
+    a = dict(q=FAKE, q_scale=None, q_dtype=0, k_payload=FAKE, k_scale=None, k_dtype=0,
+             num_pages=100, page_table=FAKE, n_slots=4, max_pages=8, block_begin=0,
+             slot_ids=FAKE, row_lens=FAKE, R=2, P=4, G=4, init=1, local=2, topk=8,
+             out_ids=FAKE, out_scores=FAKE, ws=FAKE, ws_bytes=1 << 20, stream=None)
+    a.update(over)
+    return L.idx_score_local_blocks(a["q"], a["q_scale"], a["q_dtype"], a["k_payload"],
+                                    a["k_scale"], a["k_dtype"], a["num_pages"], a["page_table"],
+                                    a["n_slots"], a["max_pages"], a["block_begin"], a["slot_ids"],
+                                    a["row_lens"], a["R"], a["P"], a["G"], a["init"], a["local"],
+                                    a["topk"], a["out_ids"], a["out_scores"], a["ws"],
+                                    a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(block_begin=-1),
+    dict(max_pages=7),          # a shard holds whole 128-token blocks
+    dict(P=8, G=4),             # more than one 16-row tile: refused in shard mode
+    dict(topk=0),
+    dict(q=None),
+])
+def test_shard_scoring_validation(L, over):
+    assert _shard(L, **over) == -1
+    assert L.idx_last_error() != b""
+
+
+def _merge(L, **over):
+    a = dict(ids=FAKE, sc=FAKE, world=3, slot_ids=FAKE, row_lens=FAKE, n_slots=4, R=2, P=4,
+             G=4, init=1, local=2, topk=8, out_ids=FAKE, out_scores=FAKE, stream=None)
+    a.update(over)
+    return L.idx_topk_merge(a["ids"], a["sc"], a["world"], a["slot_ids"], a["row_lens"],
+                            a["n_slots"], a["R"], a["P"], a["G"], a["init"], a["local"],
+                            a["topk"], a["out_ids"], a["out_scores"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(world=0),
+    dict(world=9),              # more than IDX_MAX_CP_WORLD shards
+    dict(R=-1),
+    dict(R=2049),
+    dict(P=0),
+    dict(topk=257),
+    dict(init=5, local=5, topk=8),
+    dict(n_slots=0),
+    dict(ids=None),
+    dict(out_scores=None),
+])
+def test_merge_validation(L, over):
+    assert _merge(L, **over) == -1
+    assert L.idx_last_error() != b""
+
+
+def test_merge_of_no_requests_is_a_no_op(L):
+    assert _merge(L, R=0, ids=None, sc=None, slot_ids=None, row_lens=None, out_ids=None,
+                  out_scores=None) == 0
