@@ -1,4 +1,7 @@
-// Block top-k select: one CTA (eight warps) per packed output row.
+// Block top-k select and the context-shard merge.  Three kernels: one CTA
+// (eight warps) per packed output row for long rows or few rows; one warp per
+// row for many rows of at most 256 blocks; one warp per row merging the lists
+// of context shards.
 //
 // What it computes (sglang #42614 "[AMD] MiniMax-M3 indexer CP: packed scoring
 // for EAGLE verify rows", Modifications 1 and Accuracy Tests; sglang #45451,
@@ -8,17 +11,18 @@
 // the lower block id.  Output: forced blocks ascending, chosen blocks by
 // descending score, then (-1, -inf) pads.
 //
-// How: the non-forced candidates form one contiguous id range.  Their block
-// maxima are read from L2 with many loads in flight per thread and kept in
-// shared memory as order-preserving 32-bit keys.  When there are many
-// candidates, most-significant-digit radix passes (8-bit digits starting below
-// the bits every candidate shares, one shared 256-bin histogram per digit)
-// narrow them to the keys at or above the threshold's bin, usually after one
-// pass.  Each remaining (key, id) entry is then placed by its rank among them,
-// ties going to the lower id; entries ranked c or later are dropped.  (One
-// warp sorting them with a bitonic network measured slower here, also with
-// 1024 rows in flight: its chain is longer than n threads' rank counts.)  The score
-// written out is recovered from the key, so nothing is read back from memory.
+// How (CTA per row): the non-forced candidates form one contiguous id range.
+// Their block maxima are read from L2 with as many loads in flight per thread
+// as the row needs and kept in shared memory as order-preserving 32-bit keys.
+// When there are many candidates, most-significant-digit radix passes (8-bit
+// digits starting below the bits every candidate shares, one shared 256-bin
+// histogram per digit) narrow them to the keys at or above the threshold's
+// bin, usually after one pass.  Each remaining (key, id) entry is then placed
+// by its rank among them, ties going to the lower id; entries ranked c or later
+// are dropped.  (A second pass, one warp sorting the entries with a bitonic
+// network, and several threads sharing each entry's count all measured slower
+// in the step.)  The score written out is recovered from the key, so nothing
+// is read back from memory.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
