@@ -49,11 +49,45 @@ def is_wide(spec) -> bool:
     return spec.packed_queries * spec.gqa > 16
 
 
+def code_only(text: str) -> str:
+    """C/C++ source without its comments and with every run of blank space
+    outside string and character literals made one space: what the compiler
+    sees, so an edit of comments or layout keeps a kernel's hash."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):            # a comment counts as blank space
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":                       # a literal is kept as written
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif c.isspace():
+            out.append(" ")
+            i += 1
+        else:
+            out.append(c)
+            i += 1
+        if len(out) > 1 and out[-1] == " " and out[-2] == " ":
+            out.pop()
+    return "".join(out).strip()
+
+
 def kernel_sha(wide: bool = False) -> str:
+    """Hash of the kernel sources as the compiler sees them (comments and
+    layout left out); `profiles/traffic.json` holds DRAM counters per hash."""
     h = hashlib.sha256()
     for f in (WIDE_SOURCES if wide else SCORE_SOURCES):
-        with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f)) as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,16 +1,18 @@
-// Packed index-score kernel: per-row masked q.k and per-128-token block max.
+// Packed index-score kernel: per-row masked q.k and a score per 128-token block
+// (the block max, or its log-sum-exp).
 //
 // What it computes (sglang #45451, Modifications; sglang #42614 "[AMD]
 // MiniMax-M3 indexer CP: packed scoring for EAGLE verify rows", Modifications 1):
 // the P draft rows x G heads of a request (P*G <= 16) share one 16-row dot tile,
 // so each key tile crosses HBM once per request; tile row i is (draft row i / G,
 // head i % G); the keys are read up to the group's longest row while each row
-// masks tokens at or past its own length; each row emits the max score of every
+// masks tokens at or past its own length; each row emits the score of every
 // 128-token block it covers.
 //
 // How (sm_103a):
 //  * persistent grid, one CTA per SM; the flattened (group, block) work list is
-//    split into equal contiguous ranges, one per CTA;
+//    split into equal contiguous ranges, one per CTA, except a last part that
+//    warps take one block at a time from a workspace counter;
 //  * every warp of the CTA owns its own shared-memory stages: it resolves the
 //    pages of its next blocks through the slot table, issues TMA tensor loads
 //    of the 64-token pages (128-byte or 64-byte swizzle) plus 1-D bulk copies

@@ -39,3 +39,12 @@ def test_staging_views_share_the_buffer():
     # writing through the views lands in the one buffer a single copy moves
     assert torch.equal(buf[offs[0][0]:offs[0][0] + 40].view(torch.int32), a)
     assert torch.equal(buf[offs[1][0]:offs[1][0] + 60].view(torch.float32).view(3, 5), b)
+
+
+def test_kernel_hash_ignores_comments_and_layout_only():
+    a = 'int a = 1; // note\n/* block\n note */ const char* s = "x // kept \\" /* kept */";\n'
+    b = 'int a = 1;\nconst char* s = "x // kept \\" /* kept */";  // other note\n'
+    assert bench.code_only(a) == bench.code_only(b)
+    # a change of code, or of a literal's contents, is a change
+    assert bench.code_only(a) != bench.code_only(a.replace("a = 1", "a = 2"))
+    assert bench.code_only(a) != bench.code_only(a.replace("// kept", "//  kept"))
