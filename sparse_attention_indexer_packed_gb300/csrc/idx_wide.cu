@@ -6,12 +6,11 @@
 // [128 tau, 128 tau + 128)), and tiles 2p and 2p + 1 form one "group" that
 // streams the request's keys once for both.  A 128-row x 128-token x 128-dim
 // product is one tcgen05.mma chain (M = 128, N = 128) accumulating in fp32 in
-// tensor memory, so the dot work of
-// the pages' per-request dot tile (sglang #45451, Modifications: the draft rows of
-// a request share one dot tile against its index K) is done for 128 rows at a
-// time instead of 16.  Each row keeps its own length mask and its block max (or
-// log-sum-exp), exactly as the 16-row path does; the oracle's per-row definition
-// is the same for both.
+// tensor memory, so the pages' per-request dot tile (sglang #45451,
+// Modifications: the draft rows of a request share one dot tile against its
+// index K) covers 128 rows at a time instead of 16.  Each row keeps its own
+// length mask and its block max (or log-sum-exp), exactly as the 16-row path
+// does; the oracle's per-row definition is the same for both.
 //
 // Roles inside a CTA (one CTA per SM, persistent over a contiguous range of
 // blocks of the flattened (group, block) list):
