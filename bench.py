@@ -86,7 +86,8 @@ def kernel_sha(wide: bool = False) -> str:
     layout left out); `profiles/traffic.json` holds DRAM counters per hash."""
     h = hashlib.sha256()
     for f in (WIDE_SOURCES if wide else SCORE_SOURCES):
-        with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f)) as fh:
+        with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f),
+                  encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
