@@ -1,71 +1,60 @@
 """Shared test helpers: turn a synthetic batch into the oracle's numpy inputs
 and compare CUDA-path outputs with the oracle's."""
 import numpy as np
-import torch
 
-
-def np_u8(t: torch.Tensor) -> np.ndarray:
-    return t.contiguous().view(torch.uint8).numpy()
-
-
-def np_bits16(t: torch.Tensor) -> np.ndarray:
-    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+from oracle.inputs import np_bits16, np_u8  # noqa: F401  (re-exported for the tests)
+from oracle.inputs import planes as _planes
+from oracle.inputs import step_kwargs as _step_kwargs
 
 
 def oracle_planes(batch, requests=None):
-    """Pool planes as the oracle sees them.  For NVFP4 the oracle quantises the
-    bf16 staging keys itself (never reading bytes the CUDA path wrote); with
-    ``requests`` only those requests' keys are quantised."""
-    import oracle
-    payload = np_u8(batch.payload).copy()
-    scale = None if batch.scale is None else np_u8(batch.scale).copy()
-    if batch.spec.k_dtype == "nvfp4" and batch.staging is not None and batch.staging.numel():
-        if requests is None:
-            sel = slice(None)
-            stage = batch.staging
-            rows = batch.slot_mapping.numpy()
-        else:
-            lens = batch.group_lens()
-            idx = [np.arange(batch.staging_offsets[r], batch.staging_offsets[r] + lens[r])
-                   for r in requests if batch.staging_offsets[r] >= 0]
-            sel = np.concatenate(idx) if idx else np.zeros(0, np.int64)
-            stage = batch.staging[torch.from_numpy(sel)]
-            rows = batch.slot_mapping.numpy()[sel]
-        pay, sc = oracle.formats.nvfp4_quantize(np_bits16(stage))
-        keep = rows >= 0
-        payload[rows[keep]] = pay[keep]
-        scale[rows[keep]] = sc[keep]
-    return payload, scale
+    """Pool planes as the oracle sees them (oracle.inputs.planes)."""
+    return _planes(batch, requests=requests)
 
 
 def oracle_kwargs(batch, planes=None):
-    payload, scale = planes if planes is not None else oracle_planes(batch)
-    if batch.spec.q_dtype == "bf16":
-        q = np_bits16(batch.q)
-    else:
-        q = np_u8(batch.q)
-    return dict(q=q, q_dtype=batch.spec.q_dtype,
-                q_scale=None if batch.q_scale is None else batch.q_scale.numpy().astype(np.float64),
-                payload=payload, scale=scale, k_dtype=batch.spec.k_dtype,
-                page_table=batch.page_table.numpy(), slot_ids=batch.slot_ids.numpy(),
-                row_lens=batch.row_lens.numpy(), packed_queries=batch.spec.packed_queries,
-                gqa=batch.spec.gqa, init_blocks=batch.spec.init_blocks,
-                local_blocks=batch.spec.local_blocks, topk=batch.spec.topk)
+    """index_step's arguments for the batch (oracle.inputs.step_kwargs)."""
+    return _step_kwargs(batch, pool_planes=planes)
 
 
 def score_tol(s):
-    """|delta| <= 1e-3 * (1 + |s|), the block-max score tolerance."""
+    """|delta| <= 1e-3 * (1 + |s|), the block-score tolerance."""
     return 1e-3 * (1.0 + np.abs(s))
+
+
+def near_tie_violation(bm, cands, c, diff, tol=score_tol):
+    """The id-set rule for a selection of c blocks from ``cands``.
+
+    cands: candidate block ids (forced blocks excluded); c: how many of them
+    the oracle chose; diff: the ids on which the two selections differ.  The
+    sets may differ only where the oracle's k-th and (k+1)-th candidates (its
+    last chosen and its best unchosen one, ranked by score desc, id asc) lie
+    within tolerance of each other, and then only in candidates whose oracle
+    score lies within tolerance of the k-th's.  Returns an error string or
+    None."""
+    if not diff:
+        return None
+    order = sorted(cands, key=lambda b: (-bm[b], b))
+    if c <= 0 or c >= len(order):
+        return f"id sets differ with no unchosen candidate to tie with: {sorted(diff)}"
+    s_k, s_k1 = float(bm[order[c - 1]]), float(bm[order[c]])
+    t = float(tol(s_k))
+    if abs(s_k - s_k1) > t:
+        return (f"id sets differ {sorted(diff)} but the k-th and (k+1)-th scores "
+                f"{s_k} and {s_k1} are not within tolerance")
+    for b in diff:
+        if abs(float(bm[b]) - s_k) > t:
+            return f"id sets differ beyond the near tie at block {b}: {bm[b]} vs k-th {s_k}"
+    return None
 
 
 def compare_row(ids_dev, sc_dev, ids_ref, sc_ref, blockmax_ref, init_blocks, local_blocks):
     """Compare one row's top-k output against the oracle.
 
-    IDs must be equal as sets, except that where the oracle's last-chosen and
-    best-unchosen candidate scores lie within tolerance, any choice among the
-    near-tied candidates is accepted.  Every emitted id's score must be within
-    tolerance of the oracle's block max for that id.  Returns an error string
-    or None.
+    IDs must be equal as sets, except where the oracle's k-th and (k+1)-th
+    candidate scores lie within tolerance (near_tie_violation).  Every emitted
+    id's score must be within tolerance of the oracle's block score for that
+    id.  Returns an error string or None.
     """
     ids_dev = np.asarray(ids_dev, dtype=np.int64)
     sc_dev = np.asarray(sc_dev, dtype=np.float64)
@@ -93,16 +82,8 @@ def compare_row(ids_dev, sc_dev, ids_ref, sc_ref, blockmax_ref, init_blocks, loc
     got = set(dev.tolist())
     if ref == got:
         return None
-    # near-tie exemption: differing ids must all be candidates whose oracle score is
-    # within tolerance of the selection threshold
     forced = set(range(min(init_blocks, nb))) | set(range(max(0, nb - local_blocks), nb))
     if not forced <= got:
         return "a forced block is missing"
-    chosen = [b for b in ref if b not in forced]
-    if not chosen:
-        return f"id sets differ: {sorted(got ^ ref)}"
-    thr = min(bm[b] for b in chosen)
-    for b in got ^ ref:
-        if abs(bm[b] - thr) > 2 * score_tol(thr):
-            return f"id sets differ beyond a near tie at block {b}: {bm[b]} vs threshold {thr}"
-    return None
+    cands = [b for b in range(nb) if b not in forced]
+    return near_tie_violation(bm, cands, n_ref - len(forced & ref), got ^ ref)

@@ -1,8 +1,9 @@
 """CUDA path vs the fp64 oracle on the same seeded inputs (needs a GPU).
 
 Bar: NVFP4 stored bytes bit-exact; block-max scores within 1e-3 * (1 + |s|);
-top-k id sets exact except where the oracle's last chosen and best unchosen
-candidates lie within that tolerance (tests/_util.compare_row).
+top-k id sets exact except where the oracle's k-th and (k+1)-th candidates
+lie within that tolerance, and then only in candidates within it of the k-th
+(tests/_util.compare_row).
 """
 import numpy as np
 import pytest
@@ -10,7 +11,7 @@ import torch
 
 import oracle
 import workloads
-from _util import compare_row, oracle_kwargs, oracle_planes, np_u8, score_tol
+from _util import compare_row, near_tie_violation, oracle_kwargs, oracle_planes, np_u8, score_tol
 import _gpu
 
 pytestmark = pytest.mark.gpu
@@ -186,10 +187,26 @@ def test_nvfp4_store_golden_groups():
             assert P[row, 8 * g:8 * g + 8].tolist() == pay, (c, g, P[row].tolist())
 
 
-def test_nvfp4_scores_equal_bf16_scorer_on_dequantised_cache():
-    """e2m1 x E4M3 values are exact in bf16 (ROCm/ATOM #2745, Validation): the
-    FP4 scorer must pick the same blocks as the bf16 scorer fed the dequantised
-    keys, with the same scores."""
+# Unit roundoff of one fp32 addition that truncates instead of rounding (the
+# worst a tensor core's accumulation may do): 2^-23.
+_U_TRUNC = 2.0 ** -23
+
+
+def test_nvfp4_scores_match_bf16_scorer_on_dequantised_cache():
+    """e2m1 x E4M3 values are exact in bf16 (ROCm/ATOM #2745, Validation), so the
+    FP4 scorer and the bf16 scorer fed the dequantised keys sum the same 128 exact
+    products per token.  They do not sum them in the same order: the NVFP4 path
+    feeds the f16 MMA its k elements in the order the packed bytes arrive
+    (32m + 8t + 4h + {0..3}) with the query scaled by a power of two, the bf16
+    path in natural order, and fp32 addition is not associative, so bitwise
+    equal scores cannot be promised.  What holds: each side is the exact sum
+    after at most 127 fp32 additions, each off by at most one unit in the last
+    place (2^-23 relative, even if the hardware truncates), so each differs from
+    the exact sum by at most 127 * 2^-23 * sum_d |q_d k_d| to first order, and
+    the two by twice that.  A block score is a max over tokens, so per block the
+    bound takes the largest sum_d |q_d k_d| over the block's valid tokens.
+    Every block score of every row is checked against that bound and the top-k
+    ids must be equal except at a near tie within it."""
     spec = workloads.small_spec("eq", 401, "nvfp4", "bf16", R=5, len_range=(1, 8000), topk=32)
     b = workloads.make_batch(spec)
     payload, scale = _gpu.device_planes(b)
@@ -203,8 +220,43 @@ def test_nvfp4_scores_equal_bf16_scorer_on_dequantised_cache():
     b16.payload = kb.view(torch.uint8).reshape(-1, 256)
     b16.scale = None
     out16 = _gpu.run(b16, planes=(b16.payload.cuda(), None))
-    assert np.array_equal(out4.ids, out16.ids)
-    np.testing.assert_allclose(out4.scores, out16.scores, rtol=1e-6, atol=1e-6)
+    qf = b.q.to(torch.float64).numpy()
+    pt, lens = b.page_table.numpy(), b.row_lens.numpy()
+    worst, checked, bad = 0.0, 0, []
+    for r in range(b.R):
+        slot = int(b.slot_ids[r])
+        if not 0 <= slot < b.n_slots:
+            continue
+        ext = int(lens[r].max())
+        if ext <= 0:
+            continue
+        absk = np.abs(deq[oracle.index.key_rows(pt, slot, ext)])
+        for i in range(b.M):
+            j, h = divmod(i, spec.gqa)
+            L = int(lens[r, j])
+            nb = (L + 127) // 128
+            if nb == 0:
+                continue
+            absdot = absk[:L] @ np.abs(qf[r, j, h])
+            big = np.array([absdot[128 * x:min(128 * x + 128, L)].max() for x in range(nb)])
+            bound = 2 * 127 * _U_TRUNC * big
+            s4 = out4.blockmax[r * b.M + i, :nb].astype(np.float64)
+            s16 = out16.blockmax[r * b.M + i, :nb].astype(np.float64)
+            d = np.abs(s4 - s16)
+            worst = max(worst, float((d / bound).max()))
+            checked += nb
+            if np.any(d > bound):
+                bad.append((r, i, "block score"))
+            got, want = set(out4.ids[r, i].tolist()) - {-1}, set(out16.ids[r, i].tolist()) - {-1}
+            if got != want:
+                forced = set(oracle.index.forced_blocks(nb, spec.init_blocks, spec.local_blocks))
+                cands = [x for x in range(nb) if x not in forced]
+                tol = lambda s, bd=float(bound.max()): bd
+                err = near_tie_violation(s16, cands, len(want) - len(forced), got ^ want, tol)
+                if err:
+                    bad.append((r, i, err))
+    assert checked > 0
+    assert not bad, (bad[:10], f"worst |diff| / bound = {worst:.3g}")
 
 
 def test_pad_requests_and_empty_rows():
