@@ -6,8 +6,10 @@ JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+The headline workload is timed first; the other decode workloads
+(EXTRA_WORKLOADS) follow in the same process and are reported under "extra".
 --impl reference times the CPU oracle (the plain fp64 restatement of the
-method) on a bounded sample of the same workload, on this host's cores; it is
+method) over the whole step of the same workload on this host's cores; it is
 the reference arm (the pages' own kernels are not available to run).
 Multi-GPU runs (torchrun) are independent replicas: each rank scores its own
 copy of the workload (weak scaling, no collective on the data path).
@@ -36,6 +38,8 @@ import workloads  # noqa: E402
 METRIC = "index-step µs/layer and achieved HBM GB/s (score+top-k), 16 req × 131K bf16"
 DEFAULT_WORKLOAD = "bf16_16x131k"
 PUBLISHED_US = {"bf16_16x131k": 119.1, "fp8_16x131k": 87.4}   # packed kernel, one GB300 rank
+# decode workloads timed after the headline in the same run (spec configs)
+EXTRA_WORKLOADS = ["fp8_32x524k", "fp8_16x131k", "nvfp4_64x150k"]
 BYTES_PER_TOKEN = {"bf16": 256, "fp8_e4m3": 132, "nvfp4": 72}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 L2_BYTES = 129 * 1024 * 1024
@@ -253,10 +257,10 @@ def metric_name(args) -> str:
     return f"index-step µs/layer ({args.workload}{suffix})"
 
 
-def workload_config(s, R, args, ws_n) -> dict:
-    """The workload's own keys in the JSON line's config (both arms)."""
+def workload_config(s, R, args, ws_n, workload=None) -> dict:
+    """The workload's own keys in the JSON line's config (the same on both arms)."""
     return {
-        "workload": args.workload, "requests": R, "packed_queries": s.packed_queries,
+        "workload": workload or args.workload, "requests": R, "packed_queries": s.packed_queries,
         "gqa": s.gqa, "k_dtype": s.k_dtype, "q_dtype": s.q_dtype,
         "context": (f"U[{s.len_range[0]},{s.len_range[1]}]" if s.len_range else "explicit"),
         "topk": s.topk, "init_blocks": s.init_blocks, "local_blocks": s.local_blocks,
@@ -267,6 +271,289 @@ def workload_config(s, R, args, ws_n) -> dict:
 
 def score_fn(idx, args):
     return idx.idx_score_topk_lse if args.block_score == "lse" else idx.idx_score_topk
+
+
+def percentile(xs, q):
+    """The q-quantile of xs (linear interpolation between order statistics)."""
+    ys = sorted(xs)
+    if not ys:
+        return float("nan")
+    pos = (len(ys) - 1) * q
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
+class Resident:
+    """One workload's batch resident in HBM with its outputs and workspace."""
+
+    def __init__(self, idx, spec, dev):
+        self.batch = batch = workloads.make_batch(spec)
+        s = self.spec = batch.spec
+        self.payload = batch.payload.to(dev)
+        self.scale = None if batch.scale is None else batch.scale.to(dev)
+        if s.k_dtype == "nvfp4":
+            idx.idx_store_nvfp4(batch.staging.to(dev), batch.slot_mapping.to(dev),
+                                (self.payload, self.scale))
+        self.q = batch.q.to(dev)
+        self.q_scale = None if batch.q_scale is None else batch.q_scale.to(dev)
+        self.pt = batch.page_table.to(dev)
+        self.slots = batch.slot_ids.to(dev)
+        self.lens = batch.row_lens.to(dev)
+        R, M = batch.R, batch.M
+        self.out_ids = torch.empty((R, M, s.topk), dtype=torch.int32, device=dev)
+        self.out_sc = torch.empty((R, M, s.topk), dtype=torch.float32, device=dev)
+        self.wsp = idx.alloc_workspace(R, s.packed_queries, s.gqa, batch.max_pages, device=dev)
+        self.in_bytes = (self.payload.numel() + (0 if self.scale is None else self.scale.numel()) +
+                         self.q.numel() * self.q.element_size())
+
+    def call(self, fn, dev, events=None):
+        """One step on whatever stream is current (the caller's or a capture's)."""
+        import sparse_attention_indexer_packed_gb300 as idx
+        s = self.spec
+        if events is not None:
+            idx.idx_set_kernel_events(*events)
+        fn(self.q, self.q_scale, self.payload, self.scale, s.k_dtype, self.pt, self.slots,
+           self.lens, s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, s.topk,
+           self.out_ids, self.out_sc, self.wsp, torch.cuda.current_stream(dev))
+
+
+def time_step(idx, res, fn, dev, stream, args, ws_n, min_seconds):
+    """Time the step of a resident workload.
+
+    A sample is K = args.steps steps replayed from CUDA graphs between two CUDA
+    events (workloads whose inputs fit in L2 get it flushed before every step,
+    outside the step's events).  Samples are repeated back to back until they
+    span min_seconds and number at least 100 steps; value is the median per-step
+    time over samples, max over ranks.  A second pass replays the same steps with
+    the library's events around each kernel (external event nodes of a second
+    graph) for the per-kernel durations."""
+    K = args.steps
+    n_per = max(d for d in range(1, min(K, 25) + 1) if K % d == 0)
+    reps = K // n_per
+    flush_buf = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+                 if res.in_bytes < 2 * L2_BYTES else None)
+    for _ in range(args.warmup):
+        res.call(fn, dev)
+    torch.cuda.synchronize(dev)
+    flags = idx.idx_workspace_errors(res.wsp)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during warm-up")
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain):
+        for _ in range(1 if flush_buf is not None else n_per):
+            res.call(fn, dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_per)]
+    for trio in evs:            # torch creates an event's CUDA handle on its first record()
+        for e in trio:
+            e.record(stream)
+    g_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ev):
+        for k in range(n_per):
+            if flush_buf is not None:
+                flush_l2(flush_buf)
+            res.call(fn, dev, evs[k])
+    for _ in range(2):
+        g_plain.replay()
+        g_ev.replay()
+    torch.cuda.synchronize(dev)
+    flags = idx.idx_workspace_errors(res.wsp)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} in the graph replays")
+
+    def sample(pairs):
+        """Record one sample of K steps; returns its event pairs."""
+        out = []
+        if flush_buf is None:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g_plain.replay()
+            b.record(stream)
+            out.append((a, b))
+        else:
+            for _ in range(K):
+                flush_l2(flush_buf)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g_plain.replay()
+                b.record(stream)
+                out.append((a, b))
+        pairs.append(out)
+
+    def elapsed(p):
+        return sum(a.elapsed_time(b) for a, b in p)
+
+    # one sample sets the count; then all samples run back to back, one sync
+    probe = []
+    sample(probe)
+    torch.cuda.synchronize(dev)
+    per_sample_ms = max(1e-3, elapsed(probe[0]))
+    n_samples = max(5, -(-100 // K), int(math.ceil(min_seconds * 1e3 / per_sample_ms)))
+    n_samples = min(n_samples, 20000)
+    barrier(ws_n)
+    torch.cuda.synchronize(dev)
+    samples = []
+    for _ in range(n_samples):
+        sample(samples)
+    torch.cuda.synchronize(dev)
+    barrier(ws_n)
+    step_us = [elapsed(p) * 1e3 / K for p in samples]
+    med = statistics.median(step_us)
+    value = max_over_ranks(med, ws_n, dev)
+
+    # per-kernel durations: at least 100 steps with the library's events
+    n_ev = max(reps, -(-100 // n_per))
+    score_ms, topk_ms, step_ms = [], [], []
+    for _ in range(n_ev):
+        g_ev.replay()
+        torch.cuda.synchronize(dev)
+        score_ms += [e[0].elapsed_time(e[1]) for e in evs]
+        topk_ms += [e[1].elapsed_time(e[2]) for e in evs]
+        step_ms += [e[0].elapsed_time(e[2]) for e in evs]
+    return {
+        "value_us": value, "median_us": med, "p10_us": percentile(step_us, 0.1),
+        "p90_us": percentile(step_us, 0.9), "samples": n_samples, "steps_per_sample": K,
+        "timed_steps": n_samples * K, "timed_s": sum(elapsed(p) for p in samples) / 1e3,
+        "steps_per_graph": 1 if flush_buf is not None else n_per,
+        "l2": (f"inputs larger than L2 ({res.in_bytes / 1e6:.0f} MB per step), no flush"
+               if flush_buf is None else
+               f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MB written then read, "
+               f"outside the step's events)"),
+        "score_us": statistics.fmean(score_ms) * 1e3, "topk_us": statistics.fmean(topk_ms) * 1e3,
+        "score_us_median": statistics.median(score_ms) * 1e3,
+        "evented_step_us": statistics.fmean(step_ms) * 1e3, "evented_steps": len(step_ms),
+        "flush_buf": flush_buf,
+    }
+
+
+def roofline(res, t, workload) -> dict:
+    """The dominant (score) kernel against its bound: algorithmic bytes at the
+    measured copy peak, or useful flops at the measured tensor peak, whichever
+    ideal time is longer."""
+    s = res.spec
+    ab = algorithmic_bytes(res.batch)
+    wide = is_wide(s)
+    score_s = t["score_us"] * 1e-6
+    achieved = ab["score"] / score_s / 1e9
+    peak, peak_src = measured_peak()
+    tflops = ab["flops"] / score_s / 1e12
+    tpeak, tpeak_src = measured_tensor_peak(s.k_dtype)
+    tensor_bound = ab["flops"] / (tpeak * 1e12) > ab["score"] / (peak * 1e9)
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            tr = json.load(fh).get(workload)
+        if tr and tr.get("kernel_sha") == kernel_sha(wide):
+            traffic = tr["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    out = ({"bound": "tensor", "kernel": "wide_kernel", "achieved": round(tflops, 1),
+            "peak": tpeak, "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+            "peak_source": tpeak_src, "traffic": traffic,
+            "hbm_GBps": round(achieved, 1), "hbm_frac": round(achieved / peak, 4)}
+           if tensor_bound else
+           {"bound": "hbm", "kernel": "wide_kernel" if wide else "score_kernel",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": traffic,
+            "tensor_TFLOPs": round(tflops, 1), "tensor_frac": round(tflops / tpeak, 4)})
+    out.update({
+        "algorithmic_bytes_per_launch": ab["score"],
+        "algorithmic_flops_per_launch": ab["flops"],
+        "key_reads_per_request": ab["key_reads_per_request"],
+        "score_us": round(t["score_us"], 3), "score_us_median": round(t["score_us_median"], 3),
+        "topk_us": round(t["topk_us"], 3),
+        "frac_of_8TBps": round(achieved / 8000.0, 4),
+        "step_us_with_kernel_events": round(t["evented_step_us"], 3),
+        "evented_steps": t["evented_steps"],
+    })
+    return out
+
+
+def timing_record(t) -> dict:
+    return {"median_us": round(t["median_us"], 3), "p10_us": round(t["p10_us"], 3),
+            "p90_us": round(t["p90_us"], 3), "samples": t["samples"],
+            "steps_per_sample": t["steps_per_sample"], "timed_steps": t["timed_steps"],
+            "timed_s": round(t["timed_s"], 3), "steps_per_graph": t["steps_per_graph"],
+            "l2": t["l2"],
+            "how": "value = median over samples of K steps each (CUDA graph replays between "
+                   "two CUDA events, samples back to back); score_us / topk_us: CUDA events "
+                   "the library records around each kernel (external event nodes of a "
+                   "second graph), averaged over its evented_steps"}
+
+
+def run_ablation(idx, res, dev, stream, flush_buf, n_ab):
+    """The same step with every draft row scored on its own (per-row kernel)."""
+    s = res.spec
+
+    def perrow(events=None):
+        if events is not None:
+            idx.idx_set_kernel_events(*events)
+        idx.idx_score_topk_perrow(res.q, res.q_scale, res.payload, res.scale, s.k_dtype, res.pt,
+                                  res.slots, res.lens, s.packed_queries, s.gqa, s.init_blocks,
+                                  s.local_blocks, s.topk, res.out_ids, res.out_sc, res.wsp,
+                                  torch.cuda.current_stream(dev))
+
+    for _ in range(3):
+        perrow()
+    abev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in abev:
+        e.record(stream)
+    g_ab = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ab):
+        perrow()
+    g_abev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_abev):
+        perrow(abev)
+    g_ab.replay()
+    torch.cuda.synchronize(dev)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_ab):
+        if flush_buf is not None:
+            flush_l2(flush_buf)
+        g_ab.replay()
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    ab_score = ab_step = 0.0
+    for _ in range(n_ab):
+        if flush_buf is not None:
+            flush_l2(flush_buf)
+        g_abev.replay()
+        torch.cuda.synchronize(dev)
+        ab_score += abev[0].elapsed_time(abev[1])
+        ab_step += abev[0].elapsed_time(abev[2])
+    # with the L2 flush the back-to-back pass also holds the flushes: use the
+    # evented steps then
+    ab_us = (a0.elapsed_time(a1) * 1e3 / n_ab) if flush_buf is None else ab_step / n_ab * 1e3
+    return {"variant": "per-row (each draft row its own decode row, keys read P times)",
+            "us_per_step": round(ab_us, 3), "score_us": round(ab_score / n_ab * 1e3, 3),
+            "steps": n_ab}
+
+
+def measure_extra(idx, name, args, dev, stream, ws_n, rank):
+    """Another decode workload in the same run: value, per-kernel times,
+    roofline and end-to-end step, without the ablation or the CPU baseline."""
+    spec = replica_spec(workloads.WORKLOADS[name], rank, ws_n)
+    res = Resident(idx, spec, dev)
+    fn = score_fn(idx, args)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+    t = time_step(idx, res, fn, dev, stream, args, ws_n, min_seconds=0.3)
+    clocks = sampler.stop()
+    e2e = run_e2e(idx, res.batch, res.payload, res.scale, dev, stream, args)
+    out = {"workload": name, "value": round(t["value_us"], 3), "unit": "us",
+           "config": workload_config(res.spec, res.batch.R, args, ws_n, workload=name),
+           "timing": timing_record(t), "roofline": roofline(res, t, name), "e2e": e2e,
+           "clocks": clocks, "gpu_launches": 2 * t["timed_steps"]}
+    del res, t
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -283,194 +570,29 @@ def run_ours(args):
     build_library()
 
     spec = replica_spec(workloads.WORKLOADS[args.workload], rank, ws_n)
-    batch = workloads.make_batch(spec)
-    s = batch.spec
-    payload = batch.payload.to(dev)
-    scale = None if batch.scale is None else batch.scale.to(dev)
-    if s.k_dtype == "nvfp4":
-        idx.idx_store_nvfp4(batch.staging.to(dev), batch.slot_mapping.to(dev), (payload, scale))
-        batch.staging = None
-    q = batch.q.to(dev)
-    q_scale = None if batch.q_scale is None else batch.q_scale.to(dev)
-    pt = batch.page_table.to(dev)
-    slots = batch.slot_ids.to(dev)
-    lens = batch.row_lens.to(dev)
-    R, M, topk = batch.R, batch.M, s.topk
-    out_ids = torch.empty((R, M, topk), dtype=torch.int32, device=dev)
-    out_sc = torch.empty((R, M, topk), dtype=torch.float32, device=dev)
-    wsp = idx.alloc_workspace(R, s.packed_queries, s.gqa, batch.max_pages, device=dev)
+    res = Resident(idx, spec, dev)
+    s, batch = res.spec, res.batch
     stream = torch.cuda.current_stream(dev)
-
     fn = score_fn(idx, args)
 
-    def step(events=None):
-        # on whatever stream is current: the caller's, or a graph's capture stream
-        if events is not None:
-            idx.idx_set_kernel_events(*events)
-        fn(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
-           s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, topk,
-           out_ids, out_sc, wsp, torch.cuda.current_stream(dev))
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    flags = idx.idx_workspace_errors(wsp)
-    if flags:
-        raise RuntimeError(f"device error flags {flags:#x} during warm-up")
-
-    # ---- CUDA graphs: a serving loop captures the step once and replays it, so
-    # the timed steps carry no per-call host cost.  A graph holds n_per steps
-    # (n_per divides K) and is replayed K / n_per times.
-    n_per = max(d for d in range(1, min(args.steps, 25) + 1) if args.steps % d == 0)
-    reps = args.steps // n_per
-    # inputs that fit in L2 (129 MB) get it flushed before every step (a 256 MB
-    # write and read, outside the step's own pair of events); larger inputs
-    # stream through it anyway and run back to back
-    in_bytes = (payload.numel() + (0 if scale is None else scale.numel()) +
-                q.numel() * q.element_size())
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) \
-        if in_bytes < 2 * L2_BYTES else None
-    g_plain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_plain):
-        for _ in range(1 if flush_buf is not None else n_per):
-            step()
-    # per-kernel events recorded by the library inside the graph (external nodes)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_per)]
-    for trio in evs:            # torch creates an event's CUDA handle on its first record()
-        for e in trio:
-            e.record(stream)
-    g_ev = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_ev):
-        for k in range(n_per):
-            if flush_buf is not None:
-                flush_l2(flush_buf)
-            step(evs[k])
-    for _ in range(2):
-        g_plain.replay()
-        g_ev.replay()
-    torch.cuda.synchronize(dev)
-    flags = idx.idx_workspace_errors(wsp)
-    if flags:
-        raise RuntimeError(f"device error flags {flags:#x} in the graph replays")
-
-    # ---- timed region 1: K steps back to back (graph replays) ------------------
     sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
-    barrier(ws_n)
-    torch.cuda.synchronize(dev)
-    if flush_buf is None:
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(reps):
-            g_plain.replay()
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-        run_ms = t0.elapsed_time(t1)
-    else:
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)]
-        for a_ev, b_ev in pairs:
-            flush_l2(flush_buf)
-            a_ev.record(stream)
-            g_plain.replay()
-            b_ev.record(stream)
-        torch.cuda.synchronize(dev)
-        run_ms = sum(a_ev.elapsed_time(b_ev) for a_ev, b_ev in pairs)
-    barrier(ws_n)
-    total_ms = max_over_ranks(run_ms, ws_n, dev)
-
-    # ---- timed region 2: the same K steps with the library's events around each
-    # kernel (per-kernel durations on the launching stream)
-    barrier(ws_n)
-    torch.cuda.synchronize(dev)
-    score_ms, topk_ms, step_ms = [], [], []
-    for _ in range(reps):
-        g_ev.replay()
-        torch.cuda.synchronize(dev)
-        score_ms += [e[0].elapsed_time(e[1]) for e in evs]
-        topk_ms += [e[1].elapsed_time(e[2]) for e in evs]
-        step_ms += [e[0].elapsed_time(e[2]) for e in evs]
-    barrier(ws_n)
+    t = time_step(idx, res, fn, dev, stream, args, ws_n, min_seconds=args.min_seconds)
     clocks = sampler.stop()
-    evented_ms = max_over_ranks(sum(step_ms), ws_n, dev)
+    gpu_ids = res.out_ids.cpu().numpy()
 
-    # ---- ablation: the same step with every draft row scored on its own -------
     ablation = None
     if not args.no_ablation:
-        n_ab = max(10, min(args.steps, 100))
-
-        def perrow(events=None):
-            if events is not None:
-                idx.idx_set_kernel_events(*events)
-            idx.idx_score_topk_perrow(q, q_scale, payload, scale, s.k_dtype, pt, slots, lens,
-                                      s.packed_queries, s.gqa, s.init_blocks, s.local_blocks,
-                                      topk, out_ids, out_sc, wsp, torch.cuda.current_stream(dev))
-
-        for _ in range(3):
-            perrow()
-        abev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        for e in abev:
-            e.record(stream)
-        g_ab = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_ab):
-            perrow()
-        g_abev = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_abev):
-            perrow(abev)
-        g_ab.replay()
-        torch.cuda.synchronize(dev)
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(n_ab):
-            if flush_buf is not None:
-                flush_l2(flush_buf)
-            g_ab.replay()
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        ab_score = 0.0
-        ab_step = 0.0
-        for _ in range(n_ab):
-            if flush_buf is not None:
-                flush_l2(flush_buf)
-            g_abev.replay()
-            torch.cuda.synchronize(dev)
-            ab_score += abev[0].elapsed_time(abev[1])
-            ab_step += abev[0].elapsed_time(abev[2])
-        ab_score = ab_score / n_ab * 1e3
-        # with the L2 flush the back-to-back pass also holds the flushes: use the
-        # evented steps then
-        ab_us = (a0.elapsed_time(a1) * 1e3 / n_ab) if flush_buf is None else ab_step / n_ab * 1e3
-        ablation = {"variant": "per-row (each draft row its own decode row, keys read P times)",
-                    "us_per_step": round(ab_us, 3), "score_us": round(ab_score, 3),
-                    "slowdown_vs_packed": round(ab_us / (total_ms / args.steps * 1e3), 3),
-                    "steps": n_ab}
+        ablation = run_ablation(idx, res, dev, stream, t["flush_buf"],
+                                max(10, min(args.steps, 100)))
+        ablation["slowdown_vs_packed"] = round(ablation["us_per_step"] / t["value_us"], 3)
 
     # ---- end to end through the public API with host buffers ------------------
-    e2e = run_e2e(idx, batch, payload, scale, dev, stream, args)
-
+    e2e = run_e2e(idx, batch, res.payload, res.scale, dev, stream, args)
+    rl = roofline(res, t, args.workload)
     ab = algorithmic_bytes(batch)
-    score_avg_ms = sum(score_ms) / len(score_ms)
-    wide = is_wide(s)
-    achieved = ab["score"] / (score_avg_ms * 1e-3) / 1e9
-    peak, peak_src = measured_peak()
-    tflops = ab["flops"] / (score_avg_ms * 1e-3) / 1e12
-    tpeak, tpeak_src = measured_tensor_peak(s.k_dtype)
-    # the bound is whichever ideal time is longer: bytes at the copy peak or
-    # useful flops at the tensor peak
-    tensor_bound = ab["flops"] / (tpeak * 1e12) > ab["score"] / (peak * 1e9)
-    traffic = None
-    try:
-        with open(TRAFFIC_FILE) as fh:
-            tr = json.load(fh).get(args.workload)
-        if tr and tr.get("kernel_sha") == kernel_sha(wide):
-            traffic = tr["dram_bytes_per_launch"]
-    except Exception:
-        pass
-    ms_per_step = total_ms / args.steps
-    value = ms_per_step * 1e3 / 1.0   # µs per step on each rank (replicas run concurrently)
+    value = t["value_us"]   # µs per step on each rank (replicas run concurrently)
     line = {
         "metric": metric_name(args),
         "value": round(value, 3),
@@ -478,50 +600,31 @@ def run_ours(args):
         "n_gpus": ws_n,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 6),
+        "ms_per_step": round(value / 1e3, 6),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": (round(value / PUBLISHED_US[args.workload], 4)
                         if args.workload in PUBLISHED_US else None),
         "dtype": {"bf16": "bf16", "fp8_e4m3": "e4m3", "nvfp4": "e2m1xe4m3/bf16"}[s.k_dtype],
         "data": "synthetic",
-        "config": {
-            **workload_config(s, R, args, ws_n),
-            "l2": (f"inputs larger than L2 ({ab['keys'] / 1e6:.0f} MB of keys read per step), no flush"
-                   if flush_buf is None else
-                   f"L2 flushed before every step ({L2_FLUSH_BYTES >> 20} MB written then read, "
-                   f"outside the step's events; {ab['keys'] / 1e6:.1f} MB of keys per step)"),
-            "aggregate_GBps": round(ws_n * ab["score"] / (ms_per_step * 1e-3) / 1e9, 1),
-        },
-        "roofline": {
-            **({"bound": "tensor", "kernel": "wide_kernel", "achieved": round(tflops, 1),
-                "peak": tpeak, "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
-                "peak_source": tpeak_src, "traffic": traffic,
-                "hbm_GBps": round(achieved, 1), "hbm_frac": round(achieved / peak, 4)}
-               if tensor_bound else
-               {"bound": "hbm", "kernel": "wide_kernel" if wide else "score_kernel",
-                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": traffic,
-                "tensor_TFLOPs": round(tflops, 1), "tensor_frac": round(tflops / tpeak, 4)}),
-            "algorithmic_bytes_per_launch": ab["score"],
-            "algorithmic_flops_per_launch": ab["flops"],
-            "key_reads_per_request": ab["key_reads_per_request"],
-            "score_us": round(score_avg_ms * 1e3, 3), "topk_us": round(sum(topk_ms) / len(topk_ms) * 1e3, 3),
-            "frac_of_8TBps": round(achieved / 8000.0, 4),
-            "timing": "value: K steps replayed from CUDA graphs (n_per steps per graph), no "
-                      "events between the kernels; score_us, topk_us and achieved: CUDA "
-                      "events the library records around each kernel (external event "
-                      "nodes of a second graph) in a second pass of K steps",
-            "steps_per_graph": n_per,
-            "step_us_with_kernel_events": round(evented_ms / args.steps * 1e3, 3),
-        },
+        "config": workload_config(s, batch.R, args, ws_n),
+        "timing": dict(timing_record(t),
+                       aggregate_GBps=round(ws_n * ab["score"] / (value * 1e-6) / 1e9, 1)),
+        "roofline": rl,
         "e2e": e2e,
         "ablation": ablation,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * t["timed_steps"],
         "clocks": clocks,
     }
+    del t["flush_buf"]
+    if not args.no_extra:
+        extras = [w for w in EXTRA_WORKLOADS if w != args.workload]
+        if extras:
+            del res
+            torch.cuda.empty_cache()
+            line["extra"] = [measure_extra(idx, w, args, dev, stream, ws_n, rank) for w in extras]
     if rank == 0:
-        line["cpu_baseline"] = (cpu_baseline(batch, args)
+        line["cpu_baseline"] = (cpu_baseline(batch, args, gpu_ids)
                                 if ws_n == 1 and not args.no_cpu_baseline else None)
         print(json.dumps(line), flush=True)
     if ws_n > 1:
@@ -673,79 +776,97 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
             "steps_per_graph": G, "mode": mode}
 
 
-def _oracle_sample(batch, budget_s: float, block_score: str = "max"):
-    """Time the oracle on request 0 with its rows cut to n tokens; returns
-    (seconds per token-row, n, cores)."""
-    import oracle
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from _util import oracle_kwargs
-    s = batch.spec
-    kw = dict(oracle_kwargs(batch), block_score=block_score)
-    r0 = next(r for r in range(batch.R) if batch.group_lens()[r] > 0)
-    n = 4096
-    while True:
-        lens = np.minimum(kw["row_lens"][r0:r0 + 1], n)
-        kw1 = dict(kw, q=kw["q"][r0:r0 + 1], q_scale=None if kw["q_scale"] is None else kw["q_scale"][r0:r0 + 1],
-                   slot_ids=kw["slot_ids"][r0:r0 + 1], row_lens=lens)
-        t = time.perf_counter()
-        oracle.index.index_step(**kw1)
-        dt = time.perf_counter() - t
-        tokens = int(lens.sum()) * s.gqa
-        if dt > budget_s / 4 or n >= int(kw["row_lens"][r0].max()):
-            return dt / tokens, n, dt
-        n *= 2
+def _oracle_pool(batch, block_score):
+    """The oracle's step arguments for the batch and a process pool running it on
+    every host core (oracle.pool)."""
+    import oracle.inputs
+    import oracle.pool
+    kw = dict(oracle.inputs.step_kwargs(batch), block_score=block_score)
+    return oracle.pool.OraclePool(kw)
 
 
-def _cores() -> int:
-    try:
-        from threadpoolctl import threadpool_info
-        info = threadpool_info()
-        if info:
-            return max(int(i.get("num_threads", 1)) for i in info)
-    except Exception:
-        pass
-    return os.cpu_count() or 1
+def _tokens_rows(batch, requests) -> int:
+    """Token-rows the oracle scores for these requests (rows x their lengths)."""
+    lens = batch.group_lens()
+    return int(sum(batch.row_lens[r].clamp_min(0).sum() for r in requests if lens[r] > 0)) * \
+        batch.spec.gqa
 
 
-def cpu_baseline(batch, args) -> dict:
-    per_tok, n, dt = _oracle_sample(batch, budget_s=20.0, block_score=args.block_score)
-    total_rows = int(sum(batch.row_lens[r].clamp_min(0).sum() for r in range(batch.R)
-                         if batch.group_lens()[r] > 0)) * batch.spec.gqa
-    us = per_tok * total_rows * 1e6
-    return {"value": round(us, 1), "unit": "us", "cores": _cores(), "kind": "oracle",
-            "sample": f"request 0, all {batch.M} packed rows cut to {n} tokens "
-                      f"({dt:.2f} s), scaled by token-rows to the whole step"}
+def cpu_baseline(batch, args, gpu_ids=None) -> dict:
+    """The oracle (as it stands) timed on this host's cores over the whole step:
+    every request and packed row, requests handed to single-threaded worker
+    processes.  One untimed step starts the workers; then steps are timed until
+    about 10 s of wall time (at least 2).  The untimed step's ids are compared
+    with the GPU's, row by row, as a full-size cross-check."""
+    import oracle.pool
+    with _oracle_pool(batch, args.block_score) as p:
+        ids, _ = p.step()
+        times = []
+        t_end = time.perf_counter() + 10.0
+        while len(times) < 2 or (time.perf_counter() < t_end and len(times) < 20):
+            t0 = time.perf_counter()
+            p.step()
+            times.append(time.perf_counter() - t0)
+        workers, nreq = p.workers, len(p.requests)
+    out = {"value": round(statistics.median(times) * 1e6, 1), "unit": "us", "cores": workers,
+           "kind": "oracle", "cpu_model": oracle.pool.cpu_model(),
+           "sample": (f"the whole step: all {nreq} requests with keys x {batch.M} packed rows "
+                      f"({_tokens_rows(batch, range(batch.R))} token-rows), {len(times)} timed "
+                      f"steps after one untimed one, median; {workers} single-threaded worker "
+                      f"processes, one request per task")}
+    if gpu_ids is not None:
+        same = sum(set(ids[r, i][ids[r, i] >= 0].tolist()) ==
+                   set(gpu_ids[r, i][gpu_ids[r, i] >= 0].tolist())
+                   for r in range(batch.R) for i in range(batch.M))
+        out["ids_equal_to_gpu_rows"] = f"{same}/{batch.R * batch.M}"
+    return out
 
 
 def run_reference(args):
+    """The reference arm: the oracle timed on this host's cores, W untimed and K
+    timed steps of the whole workload (every request and row), on the same
+    config, metric and unit as our arm.  Should the second warm-up step run past
+    6 s, each step is a bounded sample instead: the longest requests that fit
+    3 s, scaled by token-rows to the whole step (said in the line)."""
+    import oracle.pool
     ws_n, rank, _ = dist_env()
     if rank != 0:
         return
     spec = workloads.WORKLOADS[args.workload]
     batch = workloads.make_batch(spec)
-    budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
-    per_tok, n, dt = _oracle_sample(batch, budget_s=budget * 4, block_score=args.block_score)
-    total_rows = int(sum(batch.row_lens[r].clamp_min(0).sum() for r in range(batch.R)
-                         if batch.group_lens()[r] > 0)) * spec.gqa
-    import oracle
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from _util import oracle_kwargs
-    kw = dict(oracle_kwargs(batch), block_score=args.block_score)
-    r0 = next(r for r in range(batch.R) if batch.group_lens()[r] > 0)
-    lens = np.minimum(kw["row_lens"][r0:r0 + 1], n)
-    kw1 = dict(kw, q=kw["q"][r0:r0 + 1], q_scale=None if kw["q_scale"] is None else kw["q_scale"][r0:r0 + 1],
-               slot_ids=kw["slot_ids"][r0:r0 + 1], row_lens=lens)
-    for _ in range(args.warmup):
-        oracle.index.index_step(**kw1)
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.index.index_step(**kw1)
-    el = time.perf_counter() - t
-    tokens = int(lens.sum()) * spec.gqa
-    us = el / args.steps / tokens * total_rows * 1e6
-    cores = _cores()
-    sample = (f"per step: request 0, all {batch.M} packed rows cut to {n} tokens; "
-              f"scaled by token-rows to the whole step")
+    with _oracle_pool(batch, args.block_score) as p:
+        todo = list(p.requests)
+        p.step(todo)                       # first warm-up step (starts the workers)
+        t0 = time.perf_counter()
+        p.step(todo)                       # second warm-up step sizes the sample
+        second = time.perf_counter() - t0
+        scale = 1.0
+        if second > 6.0:
+            per_tok = second / max(1, _tokens_rows(batch, todo))
+            keep, acc = [], 0
+            for r in todo:
+                if keep and (acc + _tokens_rows(batch, [r])) * per_tok > 3.0:
+                    break
+                keep.append(r)
+                acc += _tokens_rows(batch, [r])
+            scale = _tokens_rows(batch, todo) / max(1, acc)
+            todo = keep
+        for _ in range(max(0, args.warmup - 2)):
+            p.step(todo)
+        times = []
+        for _ in range(args.steps):
+            t1 = time.perf_counter()
+            p.step(todo)
+            times.append((time.perf_counter() - t1) * scale)
+        workers = p.workers
+    us = statistics.median(times) * 1e6
+    if scale == 1.0:
+        sample = (f"each step the whole workload: {len(todo)} requests with keys x {batch.M} "
+                  f"packed rows; median of {args.steps} steps after {args.warmup} untimed; "
+                  f"{workers} single-threaded worker processes, one request per task")
+    else:
+        sample = (f"each step {len(todo)} of the requests (the longest), scaled by token-rows "
+                  f"(x{scale:.2f}) to the whole step; median of {args.steps} steps")
     line = {
         "impl": "reference",
         "metric": metric_name(args),
@@ -753,9 +874,10 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(spec, batch.R, args, ws_n),
-        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": cores, "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": workers, "kind": "oracle",
+                         "cpu_model": oracle.pool.cpu_model(), "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -763,15 +885,19 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--block-score", default="max", choices=["max", "lse"],
                     help="block score the selection ranks by (max: the headline step)")
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="timed samples of K steps are repeated until they span this long")
     ap.add_argument("--no-ablation", action="store_true", help="skip the per-row ablation timing")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle's CPU timing (profiling runs)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --workload (not the other decode workloads as well)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

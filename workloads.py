@@ -28,6 +28,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import torch
@@ -111,7 +112,30 @@ class Batch:
         return sum(min(L, self.max_pages * PAGE) for L in self.group_lens()) * per_tok
 
 
-def _e4m3_rows(gen: torch.Generator, n: int, chunk: int = 1 << 16):
+_CHUNK = 1 << 16   # rows drawn by one chunk generator
+
+
+def _chunked(gen: torch.Generator, n: int, fill) -> None:
+    """Run fill(chunk_generator, a, b) over rows [a, b) in chunks of _CHUNK rows,
+    on a thread pool.  Every chunk draws from its own generator, seeded from one
+    number taken from `gen`, so the bytes do not depend on the thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+    base = int(torch.randint(0, 2 ** 62, (1,), generator=gen))
+    spans = [(c, a, min(n, a + _CHUNK)) for c, a in enumerate(range(0, n, _CHUNK))]
+
+    def one(span):
+        c, a, b = span
+        fill(torch.Generator().manual_seed((base + 1000003 * c) % (2 ** 63)), a, b)
+
+    if len(spans) <= 1:
+        for sp in spans:
+            one(sp)
+        return
+    with ThreadPoolExecutor(max_workers=min(len(spans), os.cpu_count() or 1)) as ex:
+        list(ex.map(one, spans))
+
+
+def _e4m3_rows(gen: torch.Generator, n: int):
     """n vectors v ~ N(0,1)^D, each scaled so its amax maps to 448.
 
     Returns (codes uint8 [n, D], scale fp32 [n]) with value = code * scale.
@@ -119,21 +143,36 @@ def _e4m3_rows(gen: torch.Generator, n: int, chunk: int = 1 << 16):
     """
     codes = torch.empty((n, DIM), dtype=torch.uint8)
     scales = torch.empty((n,), dtype=torch.float32)
-    for a in range(0, n, chunk):
-        b = min(n, a + chunk)
-        v = torch.randn((b - a, DIM), generator=gen, dtype=torch.float32)
+
+    def fill(g, a, b):
+        v = torch.randn((b - a, DIM), generator=g, dtype=torch.float32)
         amax = v.abs().amax(dim=1).clamp_min(1e-30)
         x = (v * (448.0 / amax)[:, None]).clamp(-448.0, 448.0)
         codes[a:b] = x.to(torch.float8_e4m3fn).view(torch.uint8)
         scales[a:b] = amax / 448.0
+
+    _chunked(gen, n, fill)
     return codes, scales
 
 
-def _bf16_rows(gen: torch.Generator, n: int, chunk: int = 1 << 18) -> torch.Tensor:
+def _bf16_rows(gen: torch.Generator, n: int) -> torch.Tensor:
     out = torch.empty((n, DIM), dtype=torch.bfloat16)
-    for a in range(0, n, chunk):
-        b = min(n, a + chunk)
-        out[a:b] = torch.randn((b - a, DIM), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+    def fill(g, a, b):
+        out[a:b] = torch.randn((b - a, DIM), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+    _chunked(gen, n, fill)
+    return out
+
+
+def _byte_rows(gen: torch.Generator, n: int, width: int, hi: int) -> torch.Tensor:
+    """uint8 [n, width], each byte uniform in [0, hi)."""
+    out = torch.empty((n, width), dtype=torch.uint8)
+
+    def fill(g, a, b):
+        out[a:b] = torch.randint(0, hi, (b - a, width), generator=g, dtype=torch.uint8)
+
+    _chunked(gen, n, fill)
     return out
 
 
@@ -191,9 +230,9 @@ def make_batch(spec: Spec) -> Batch:
         payload = codes
         scale = sc.view(torch.uint8).reshape(rows, 4).clone()
     elif spec.k_dtype == "nvfp4":
-        payload = torch.randint(0, 256, (rows, 64), generator=gen, dtype=torch.uint8)
+        payload = _byte_rows(gen, rows, 64, 256)
         # junk scale bytes stay finite: 0x7F / 0xFF are the E4M3 NaN codes
-        scale = torch.randint(0, 0x7F, (rows, 8), generator=gen, dtype=torch.uint8)
+        scale = _byte_rows(gen, rows, 8, 0x7F)
         # the step's keys arrive as bf16 token-major staging + a slot mapping
         maps = []
         staging_offsets = []
