@@ -168,7 +168,11 @@ IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queri
  *                        (IDX_DEVERR_*) of the last call and the state of the
  *                        kernel's dynamic work counter, which every call leaves
  *                        ready for the next one (a fresh workspace simply runs
- *                        its first call with a static schedule).
+ *                        its first call with a static schedule).  Calls that may
+ *                        overlap on the GPU (on different streams, or from
+ *                        different host threads without ordering) must not share
+ *                        a workspace: they race on its block scores, its error
+ *                        flags and the work counter.
  * Output row i of request r: its forced blocks in ascending id order, then the chosen
  * blocks by descending score (ties to the lower id), then (-1, -inf) pads.  Scores are
  * raw q.k block maxima (fp8: code dot products times q_scale times the key's scale).
@@ -304,8 +308,10 @@ IDX_API int idx_set_kernel_events(void* score_begin, void* score_end, void* topk
  * any stream capture.  All calls share the one array and it keeps the last call's
  * contents (each call rewrites what it reads): calls that overlap on
  * the GPU — on different streams, or from different host threads — race on it and
- * must be serialised by the caller.  The device error flags of this variant are
- * not exposed.
+ * must be serialised by the caller.  The device error flags of the last call on
+ * the current device are read with idx_noalloc_errors.  If the device's context
+ * is torn down and made anew (cudaDeviceReset), the next call looks the address
+ * up again.
  */
 #define IDX_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
 IDX_API int idx_score_topk_noalloc(const void* q, const float* q_scale, int q_dtype,
@@ -315,6 +321,13 @@ IDX_API int idx_score_topk_noalloc(const void* q, const float* q_scale, int q_dt
                                    const int32_t* row_lens, int num_requests, int packed_queries,
                                    int gqa, int init_blocks, int local_blocks, int topk,
                                    int32_t* out_ids, float* out_scores, void* stream);
+
+/* idx_noalloc_errors — the device error flags (IDX_DEVERR_*) of the last
+ * idx_score_topk_noalloc call on the current device, read from the fixed scratch
+ * array's header (syncs on stream; allocates nothing).  No counterpart on the
+ * pages: it is the no-allocation variant's idx_workspace_errors.
+ *   flags (host): receives the IDX_DEVERR_* bits. */
+IDX_API int idx_noalloc_errors(void* stream, uint32_t* flags);
 
 /* idx_set_wait_limit_ns — limit (nanoseconds, process-wide) of every pipeline wait in
  * the score kernels; 0 restores the default of 2 s.  A wait that runs past it ends

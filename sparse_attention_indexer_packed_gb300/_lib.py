@@ -68,6 +68,7 @@ _SIGNATURES = {
     "idx_set_kernel_events": (_I, [_P, _P, _P]),
     "idx_set_grid_limit": (_I, [_I]),
     "idx_workspace_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "idx_noalloc_errors": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
 }
 
 
@@ -301,4 +302,11 @@ def idx_workspace_errors(workspace: torch.Tensor, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().idx_workspace_errors(_dev(workspace, "workspace"), _stream_ptr(stream),
                                       ctypes.byref(v)), "idx_workspace_errors")
+    return int(v.value)
+
+
+def idx_noalloc_errors(stream=None) -> int:
+    """Device error flags of the last idx_score_topk_noalloc call on this device."""
+    v = ctypes.c_uint32(0)
+    _check(lib().idx_noalloc_errors(_stream_ptr(stream), ctypes.byref(v)), "idx_noalloc_errors")
     return int(v.value)

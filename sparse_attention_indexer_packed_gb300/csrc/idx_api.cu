@@ -327,7 +327,14 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   ta.block_off = sa.block_off;
   ta.shard = sa.shard;
   e = idx::launch_topk(ta, st);
-  if (e != cudaSuccess) return cuda_fail(e, "launching the top-k kernel");
+  if (e != cudaSuccess) {
+    // the top-k kernel is what leaves the dynamic-schedule counter at zero and
+    // tags it so; without it the counter may be left nonzero, so drop the tag
+    // and the next call on this workspace schedules statically
+    cudaGetLastError();
+    (void)cudaMemsetAsync(ws + idx::kTagOff, 0, sizeof(unsigned long long), st);
+    return cuda_fail(e, "launching the top-k kernel");
+  }
   if (ev[2] && (e = record_event(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
   return IDX_OK;
 }
