@@ -41,6 +41,10 @@ namespace {
 constexpr uint32_t kErrBadPage = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 constexpr uint32_t kErrLenClamped = 4u;
+// Static blocks per warp whose pages are brought into L2 before the
+// programmatic wait, for calls of at most kHintGroups groups.
+constexpr int kPrefetchUnits = 2;
+constexpr int kHintGroups = 256;
 
 // Warps and stages per key format.  Every warp is a consumer that also issues
 // the copies for its own stages (SPW stages per warp, S = NC * SPW in all).
@@ -92,7 +96,8 @@ struct Layout {
   static constexpr int kBarOff = kScaleOff + S * kStageScale;        // full[S]
   static constexpr int kCtlOff = kBarOff + S * 8;                    // control words
   static constexpr int kGroupOff = kCtlOff + 64;                     // group table
-  static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
+  static constexpr int kHintOff = kGroupOff + (2 * kMaxGroups + 1) * 4;  // hint table
+  static constexpr int kBytes = kHintOff + (2 * kHintGroups + 4) * 4;
   static constexpr int kSmemBytes = kBytes + 1024;                   // + alignment slack
   static constexpr int kThreads = 32 * NC;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -117,7 +122,16 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// A load of the call's inputs.  kHint: read before the programmatic wait, when
+// the earlier work may still be writing them, so through L2 only (ld.global.cg):
+// a line cached in L1 there could be returned stale by a read after the wait.
+template <bool kHint = false>
+__device__ __forceinline__ int ld_in(const int* p) {
+  return kHint ? __ldcg(p) : __ldg(p);
+}
+
 // Geometry of scoring group v (a request when packed, a draft row when per-row).
+template <bool kHint = false>
 __device__ Group group_info(const ScoreArgs& a, int v) {
   Group g;
   int ext = 0;
@@ -126,14 +140,14 @@ __device__ Group group_info(const ScoreArgs& a, int v) {
     const int j = v - g.r * a.P;
     g.base_row = g.r * a.M + j * a.G;
     g.nrows = a.G;
-    ext = __ldg(a.row_lens + v);
+    ext = ld_in<kHint>(a.row_lens + v);
   } else {
     g.r = v;
     g.base_row = v * a.M;
     g.nrows = a.M;
-    for (int j = 0; j < a.P; ++j) ext = max(ext, __ldg(a.row_lens + v * a.P + j));
+    for (int j = 0; j < a.P; ++j) ext = max(ext, ld_in<kHint>(a.row_lens + v * a.P + j));
   }
-  g.slot = __ldg(a.slot_ids + g.r);
+  g.slot = ld_in<kHint>(a.slot_ids + g.r);
   const bool pad = g.slot < 0 || g.slot >= a.n_slots;
   ext = clamp_len(ext, token_cap(a));
   g.extent = pad ? 0 : max(ext, 0);
@@ -437,7 +451,7 @@ struct BlockScorer<kNvfp4> {
     const uint32_t th = (uint32_t)(t >> 1);
     // byte selectors {th, th, 2+th, 2+th}: duplicate the scale of group 2m + th
     const uint32_t sel = th | (th << 4) | ((2 + th) << 8) | ((2 + th) << 12);
-#pragma unroll 2
+#pragma unroll 16  // whole block: measured 3-4% faster than two slices at a time
     for (int nt = 0; nt < 16; ++nt) {
       // B operand: this lane's ldmatrix row address (token nt*8 + rr, chunk m)
       const int j = nt * 8 + rr;
@@ -512,6 +526,43 @@ __device__ __forceinline__ int load_page(const ScoreArgs& a, const int* gpre, co
   return p;
 }
 
+// Page ids of block b of group v as a prefetch hint (no flags; -1: none or
+// out of range).  Lanes 0 and 1 load one page-table entry each.
+__device__ __forceinline__ int hint_page(const ScoreArgs& a, const int* gpre, const int* gslot,
+                                         int v, int b, int lane) {
+  int p = -1;
+  if (lane < 2) {
+    const int word = gslot[v];
+    const int slot = word & 0x7fffffff;
+    const bool last = b == gpre[v + 1] - gpre[v] - 1;
+    if ((lane == 0 || !(last && word < 0)) && slot < a.n_slots && 2 * b + lane < a.max_pages) {
+      p = ld_in<true>(a.page_table + (size_t)slot * a.max_pages + 2 * b + lane);
+      if (p < 0 || p >= a.num_pages) p = -1;
+    }
+  }
+  return p;
+}
+
+// Bring one unit's pages (payload and scales) into L2 (lane 0 only).
+template <int KF>
+__device__ __forceinline__ void prefetch_unit(const ScoreArgs& a, const CUtensorMap* map, int p0,
+                                              int p1) {
+  using L = Layout<KF>;
+  const int pg[2] = {p0, p1};
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    if (pg[pp] < 0) continue;
+    const int y = pg[pp] * kPage;
+    if (KF == kBf16) {
+      tma_prefetch_2d(map, 0, y);
+      tma_prefetch_2d(map, 64, y);
+    } else {
+      tma_prefetch_2d(map, 0, y);
+      bulk_prefetch_l2(a.k_scale + (size_t)pg[pp] * L::kPageScale, L::kPageScale);
+    }
+  }
+}
+
 // Issue the copies of one unit into stage s (lane 0 only).
 template <int KF>
 __device__ __forceinline__ void issue_unit(const ScoreArgs& a, const CUtensorMap* map,
@@ -538,6 +589,70 @@ __device__ __forceinline__ void issue_unit(const ScoreArgs& a, const CUtensorMap
       tma_load_2d(dst + pp * C::kPagePayload, map, 0, y, full);
       bulk_load(sdst + pp * L::kPageScale, a.k_scale + (size_t)pg[pp] * L::kPageScale,
                 L::kPageScale, full);
+    }
+  }
+}
+
+// The shared group table, built by the calling warp: pre[v] = first unit of
+// group v (prefix sum of the groups' block counts), pre[V] = units of the call,
+// slot[v] = the group's slot with bit 31 set when its last block needs one
+// page; ctl[0..2] = units, first dynamically scheduled unit, dynamic schedule
+// on.  hint: built before the programmatic wait from inputs that may still
+// change (read through L2 only); only pre, slot and ctl[0..1] are written.
+template <int KF, bool hint>
+__device__ __forceinline__ void build_groups(const ScoreArgs& a, int* pre, int* slot,
+                                             volatile int* ctl, unsigned int* cta_flags, int V,
+                                             int lane) {
+  // read up front, so its round trip overlaps the row-length loads
+  const bool tag_ok = lane == 0 && (hint ? __ldcg(a.sched_tag) : *a.sched_tag) == kSchedTag;
+  int run = 0;
+  bool clamped = false;
+  for (int v0 = 0; v0 < V; v0 += 32) {
+    const int v = v0 + lane;
+    int nbk = 0, word = 0;
+    if (v < V) {
+      const Group gi = group_info<hint>(a, v);
+      nbk = gi.nbk;
+      const int rem = gi.extent - (a.block_off + nbk - 1) * kBlock;  // tokens in the last block
+      word = (nbk > 0 ? gi.slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
+      if (!hint && blockIdx.x == 0 && !a.shard && gi.slot >= 0 && gi.slot < a.n_slots) {
+        const int j0 = a.perrow ? v - gi.r * a.P : 0, j1 = a.perrow ? j0 + 1 : a.P;
+        for (int j = j0; j < j1; ++j)
+          clamped |= __ldg(a.row_lens + gi.r * a.P + j) > a.max_pages * kPage;
+      }
+    }
+    int incl = nbk;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (v < V) {
+      pre[v] = run + incl - nbk;
+      slot[v] = word;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  clamped = __any_sync(0xffffffffu, clamped);
+  if (lane == 0) {
+    pre[V] = run;
+    // the last part of the blocks is handed out at run time, which evens out
+    // the CTAs' finish times: an eighth from ~600 blocks per CTA, a quarter
+    // from 64 (measured best on 16 x 131K bf16 / fp8 calls); NVFP4 calls
+    // below 600 stay static, since a block from another request costs a
+    // query-tile conversion there.  Only when a previous call left the
+    // counter at zero (its tag says so).
+    const int grid = (int)gridDim.x;
+    int share = 0;  // 1 / share of the blocks is dynamic
+    if (tag_ok) {
+      if (run >= 600 * grid) share = 8;
+      else if (KF != kNvfp4 && run >= 64 * grid) share = 4;
+    }
+    ctl[0] = run;
+    ctl[1] = share ? run - run / share : run;
+    if (!hint) {
+      ctl[2] = share ? 1 : 0;
+      *cta_flags = clamped ? kErrLenClamped : 0u;
     }
   }
 }
@@ -571,78 +686,78 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     fence_barrier_init();
   }
   if (threadIdx.x == 0) prefetch_tensormap(&payload_map);
-  // launched as a programmatic dependent of whatever ran before on the stream:
-  // everything above touches only this CTA; from here on inputs are read and
-  // the workspace written, so wait for that work to complete
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- group table: block prefix sums and slots of every group -------------
+  // The kernel is launched as a programmatic dependent of whatever ran before
+  // on the stream, so it may start while that work still runs: inputs are
+  // read and the workspace written only after griddepcontrol.wait.  Warp 1
+  // waits and builds the real table.  Meanwhile the other warps read the
+  // inputs as they stand, as a hint (through L2 only): warp 0 builds a hint
+  // table of the groups, the others bring every request's page-table row into
+  // L2 (one 128-byte line per thread), and then each warp brings the pages of
+  // its first static blocks into L2.  A prefetch moves nothing into this CTA
+  // and L2 is coherent, so a stale hint costs only bandwidth.  When nothing
+  // ran before, the hint work overlaps warp 1's and costs no time.
+  // NVFP4 calls are bound by the key decode, not by HBM, and measured slower
+  // with the hint work: they wait first and warm only the page table.
   const int V = a.perrow ? a.R * a.P : a.R;
-  if (warp == 0) {
-    // read up front, so its round trip overlaps the row-length loads
-    const bool tag_ok = lane == 0 && *a.sched_tag == kSchedTag;
-    int run = 0;
-    bool clamped = false;
-    for (int v0 = 0; v0 < V; v0 += 32) {
-      const int v = v0 + lane;
-      int nbk = 0, word = 0;
-      if (v < V) {
-        const Group gi = group_info(a, v);
-        nbk = gi.nbk;
-        const int rem = gi.extent - (a.block_off + nbk - 1) * kBlock;  // tokens in the last block
-        word = (nbk > 0 ? gi.slot : 0) | ((nbk > 0 && rem <= kPage) ? (int)0x80000000 : 0);
-        if (blockIdx.x == 0 && !a.shard && gi.slot >= 0 && gi.slot < a.n_slots) {
-          const int j0 = a.perrow ? v - gi.r * a.P : 0, j1 = a.perrow ? j0 + 1 : a.P;
-          for (int j = j0; j < j1; ++j)
-            clamped |= __ldg(a.row_lens + gi.r * a.P + j) > a.max_pages * kPage;
+  if (KF == kNvfp4) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (warp == 1) {
+      build_groups<KF, false>(a, gpre, gslot, ctl, cta_flags, V, lane);
+    } else if (warp >= 2) {
+      const int lines_per = (a.max_pages + 31) / 32;
+      const int nthr = (int)gridDim.x * (NC - 2) * 32;
+      const int gt = ((int)blockIdx.x * (NC - 2) + warp - 2) * 32 + lane;
+      if (a.R * lines_per <= nthr && gt < a.R * lines_per) {
+        const int r = gt / lines_per, line = gt - r * lines_per;
+        const int slot = __ldg(a.slot_ids + r);
+        if (slot >= 0 && slot < a.n_slots)
+          prefetch_l2(a.page_table + (size_t)slot * a.max_pages + (size_t)line * 32);
+      }
+    }
+  } else if (warp == 1) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    build_groups<KF, false>(a, gpre, gslot, ctl, cta_flags, V, lane);
+  } else {
+    int* hpre = reinterpret_cast<int*>(smem + L::kHintOff);  // [V + 1]
+    int* hslot = hpre + kHintGroups + 1;                     // [V]
+    volatile int* hctl = hslot + kHintGroups;                // units, first dynamic unit
+    const bool hinted = V <= kHintGroups;
+    if (warp == 0) {
+      if (hinted) build_groups<KF, true>(a, hpre, hslot, hctl, nullptr, V, lane);
+    } else {
+      const int lines_per = (a.max_pages + 31) / 32;
+      const int nthr = (int)gridDim.x * (NC - 2) * 32;
+      const int gt = ((int)blockIdx.x * (NC - 2) + warp - 2) * 32 + lane;
+      if (a.R * lines_per <= nthr && gt < a.R * lines_per) {
+        const int r = gt / lines_per, line = gt - r * lines_per;
+        const int slot = ld_in<true>(a.slot_ids + r);
+        if (slot >= 0 && slot < a.n_slots)
+          prefetch_l2(a.page_table + (size_t)slot * a.max_pages + (size_t)line * 32);
+      }
+    }
+    // every warp but warp 1: the hint table is complete
+    asm volatile("bar.sync 1, %0;" ::"r"((NC - 1) * 32) : "memory");
+    if (hinted) {
+      const int Uh = hctl[0], Ush = hctl[1];
+      const int sh0 = (int)((long long)Ush * blockIdx.x / gridDim.x);
+      const int sh1 = (int)((long long)Ush * (blockIdx.x + 1) / gridDim.x);
+      // the CTA's first NC * kPrefetchUnits static units (warp w's j-th block is
+      // unit sh0 + w + j NC), spread over the NC - 1 warps here
+      const int rank = warp == 0 ? 0 : warp - 1;
+      for (int k = rank; k < NC * kPrefetchUnits; k += NC - 1) {
+        const int u = sh0 + k;
+        if (u < sh1 && u < Uh) {
+          int v, b;
+          locate(hpre, V, u, v, b);
+          const int pg = hint_page(a, hpre, hslot, v, b, lane);
+          const int p0 = __shfl_sync(0xffffffffu, pg, 0), p1 = __shfl_sync(0xffffffffu, pg, 1);
+          if (lane == 0) prefetch_unit<KF>(a, &payload_map, p0, p1);
         }
       }
-      int incl = nbk;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (v < V) {
-        gpre[v] = run + incl - nbk;
-        gslot[v] = word;
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    clamped = __any_sync(0xffffffffu, clamped);
-    if (lane == 0) {
-      gpre[V] = run;
-      // the last part of the blocks is handed out at run time, which evens out
-      // the CTAs' finish times: an eighth from ~600 blocks per CTA, a quarter
-      // from 64 (measured best on 16 x 131K bf16 / fp8 calls); NVFP4 calls
-      // below 600 stay static, since a block from another request costs a
-      // query-tile conversion there.  Only when a previous call left the
-      // counter at zero (its tag says so).
-      const int grid = (int)gridDim.x;
-      int share = 0;  // 1 / share of the blocks is dynamic
-      if (tag_ok) {
-        if (run >= 600 * grid) share = 8;
-        else if (KF != kNvfp4 && run >= 64 * grid) share = 4;
-      }
-      ctl[0] = run;
-      ctl[1] = share ? run - run / share : run;
-      ctl[2] = share ? 1 : 0;
-      *cta_flags = clamped ? kErrLenClamped : 0u;
-    }
-  } else {
-    // meanwhile the other warps of the grid bring every request's page-table
-    // row into L2 (one 128-byte line per thread), so each warp's first page
-    // lookup after the table is an L2 hit rather than a DRAM (and TLB) miss;
-    // skipped when the table is wider than the grid's threads
-    const int lines_per = (a.max_pages + 31) / 32;
-    const int nthr = (int)gridDim.x * (NC - 1) * 32;
-    const int gt = ((int)blockIdx.x * (NC - 1) + warp - 1) * 32 + lane;
-    if (a.R * lines_per <= nthr && gt < a.R * lines_per) {
-      const int r = gt / lines_per, line = gt - r * lines_per;
-      const int slot = __ldg(a.slot_ids + r);
-      if (slot >= 0 && slot < a.n_slots)
-        prefetch_l2(a.page_table + (size_t)slot * a.max_pages + (size_t)line * 32);
-    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
   }
   __syncthreads();
   // the top-k kernel may be scheduled now; it waits for this grid's completion
