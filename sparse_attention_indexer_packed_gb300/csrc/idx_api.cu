@@ -300,11 +300,6 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   }
   cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
   g_ev[0] = g_ev[1] = g_ev[2] = nullptr;
-  if (ev[0] && (e = record_event(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
-  e = wide ? idx::launch_wide(k_dtype, block_score, sa, map, qmap, st)
-           : idx::launch_score(k_dtype, block_score, sa, map, st);
-  if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
-  if (ev[1] && (e = record_event(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
 
   idx::TopkArgs ta;
   ta.blockmax = sa.blockmax;
@@ -326,6 +321,30 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   ta.topk = topk;
   ta.block_off = sa.block_off;
   ta.shard = sa.shard;
+#if IDX_FUSED_TOPK
+  const bool fused = !wide && !shard && !perrow;
+  sa.fused = fused ? 1 : 0;
+  if (fused) {
+    sa.topk = ta;
+    sa.arrive = reinterpret_cast<uint32_t*>(ws + idx::kArriveOff);
+    sa.depart = reinterpret_cast<uint32_t*>(ws + idx::kDepartOff);
+    // the grid barrier's counters must start at zero whatever the workspace
+    // held before (the dynamic schedule's tag is dropped with them)
+    e = cudaMemsetAsync(ws + idx::kSchedOff, 0, idx::kFlagBytesOff - idx::kSchedOff, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace counters");
+  }
+#else
+  const bool fused = false;
+#endif
+  if (ev[0] && (e = record_event(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
+  e = wide ? idx::launch_wide(k_dtype, block_score, sa, map, qmap, st)
+           : idx::launch_score(k_dtype, block_score, sa, map, st);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
+  if (ev[1] && (e = record_event(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
+  if (fused) {
+    if (ev[2] && (e = record_event(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
+    return IDX_OK;
+  }
   e = idx::launch_topk(ta, st);
   if (e != cudaSuccess) {
     // the top-k kernel is what leaves the dynamic-schedule counter at zero and

@@ -21,6 +21,8 @@ constexpr int kMaxTopk = 256; // largest topk a call may ask for
 constexpr int kHeaderBytes = 1024;
 constexpr int kSchedOff = 8;
 constexpr int kTagOff = 16;
+constexpr int kArriveOff = 24;  // in-kernel selection only: grid barrier counters
+constexpr int kDepartOff = 28;
 constexpr int kFlagBytesOff = 64;
 constexpr int kMaxScoreCtas = kHeaderBytes - kFlagBytesOff;
 constexpr unsigned long long kSchedTag = 0x5CEDC0DE1DC0FFEEull;
@@ -33,6 +35,34 @@ constexpr int kMaxGroups = 2048;
 enum KeyFormat : int { kBf16 = 0, kFp8 = 1, kNvfp4 = 2 };
 // Block scores: the block's largest score, or the log-sum-exp of its scores.
 enum BlockScore : int { kBlockMax = 0, kBlockLse = 1 };
+
+struct TopkArgs {
+  const float* blockmax;       // [R*M][nb_cap]
+  const int32_t* slot_ids;
+  const int32_t* row_lens;
+  int32_t* out_ids;            // [R*M][topk]
+  float* out_scores;
+  uint32_t* sched_counter;     // reset to zero for the next call
+  unsigned long long* sched_tag;
+  int n_slots, max_pages, nb_cap;
+  int R, P, G, M;
+  int init_blocks, local_blocks, topk;
+  int block_off;               // first global block the workspace's block 0 stands for
+  int shard;                   // 1: select within the shard [block_off, block_off + nb_cap)
+};
+
+// Selection inside the score kernel instead of the separate top-k kernel: one
+// launch per step, the score CTAs meet at a grid barrier (bounded wait) and
+// then select the rows, CTA k taking rows k, k + grid, ...  Off: measured
+// slower on every decode workload (one GB300, graph replays: bf16 16 x 131K
+// 83.2 -> 90.3 us a step, fp8 16 x 131K 54.2 -> 61.2, NVFP4 64 x 150K
+// 157.8 -> 182.4, fp8 32 x 524K 330.9 -> 353.8, before the per-call counter
+// reset this build also needs), since each SM then selects its rows in turn
+// with one score CTA and the next step cannot start under the selection.
+// Build with -DIDX_FUSED_TOPK=1 to try it.
+#ifndef IDX_FUSED_TOPK
+#define IDX_FUSED_TOPK 0
+#endif
 
 // Arguments of one scoring pass.  A "group" is the set of tile rows that share
 // one read of the keys: a whole request when packed, one draft row when per-row.
@@ -57,22 +87,14 @@ struct ScoreArgs {
   int shard;                   // 1: the page table holds one context shard of each request
   unsigned long long wait_ns;  // limit of each pipeline wait before IDX_DEVERR_TIMEOUT
   int stall_test;              // diagnostic: one role per CTA waits on a barrier nothing completes
+#if IDX_FUSED_TOPK
+  int fused;                   // 1: select in this kernel (16-row packed whole-context calls)
+  TopkArgs topk;               // the selection the CTAs run after a grid barrier
+  uint32_t* arrive;            // grid barrier: CTAs arrived (zero between calls)
+  uint32_t* depart;            // CTAs done selecting; the last resets both counters
+#endif
 };
 
-struct TopkArgs {
-  const float* blockmax;       // [R*M][nb_cap]
-  const int32_t* slot_ids;
-  const int32_t* row_lens;
-  int32_t* out_ids;            // [R*M][topk]
-  float* out_scores;
-  uint32_t* sched_counter;     // reset to zero for the next call
-  unsigned long long* sched_tag;
-  int n_slots, max_pages, nb_cap;
-  int R, P, G, M;
-  int init_blocks, local_blocks, topk;
-  int block_off;               // first global block the workspace's block 0 stands for
-  int shard;                   // 1: select within the shard [block_off, block_off + nb_cap)
-};
 
 // Merge of context shards' candidate lists: cand_* are [world][R*M][topk].
 struct MergeArgs {

@@ -33,6 +33,9 @@
 
 #include "idx_internal.cuh"
 #include "idx_ptx.cuh"
+#if IDX_FUSED_TOPK
+#include "idx_select.cuh"
+#endif
 
 namespace idx {
 
@@ -906,6 +909,51 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     a.err_bytes[blockIdx.x] = (uint8_t)*cta_flags;
     if (blockIdx.x == 0) *a.err_count = gridDim.x;
   }
+#if IDX_FUSED_TOPK
+  if (!a.fused) return;
+  // ---- selection in this kernel: a grid barrier (every CTA of the persistent
+  // grid is resident: one per SM), then row k is selected by CTA k % grid with
+  // the block scores read from L2; the last CTA out resets the counters ------
+  volatile int* go = ctl + 12;  // ctl[8..9] hold the stall test's barrier
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(a.arrive, 1u);
+    const uint64_t t0 = global_timer_ns();
+    int ok = 1;
+    for (uint32_t it = 0;; ++it) {
+      uint32_t n;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(n) : "l"(a.arrive) : "memory");
+      if (n >= gridDim.x) break;
+      if ((it & 15u) == 15u && global_timer_ns() - t0 > a.wait_ns) {
+        ok = 0;
+        break;
+      }
+    }
+    if (!ok) a.err_bytes[blockIdx.x] = (uint8_t)(*cta_flags | kErrTimeout);
+    *go = ok;
+  }
+  __syncthreads();
+  if (*go) {
+    const TopkArgs& ta = a.topk;
+    for (int row = blockIdx.x; row < ta.R * ta.M; row += gridDim.x) {
+      const int r = row / ta.M;
+      const sel::RowPlan pl = sel::row_plan(ta, r, row - r * ta.M);
+      sel::row_pads<L::kThreads>(ta, row, pl, threadIdx.x);
+      sel::row_select<L::kThreads, true>(ta, row, pl, smem, threadIdx.x);
+      __syncthreads();
+    }
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.depart, 1u) == gridDim.x - 1) {
+      *reinterpret_cast<volatile uint32_t*>(a.arrive) = 0u;
+      *reinterpret_cast<volatile uint32_t*>(a.depart) = 0u;
+      *reinterpret_cast<volatile uint32_t*>(a.sched_counter) = 0u;
+      __threadfence();
+      *reinterpret_cast<volatile unsigned long long*>(a.topk.sched_tag) = kSchedTag;
+    }
+  }
+#endif
 }
 
 std::atomic<int> g_grid_limit{0};
