@@ -177,6 +177,7 @@ __device__ __forceinline__ float fmax_finite(float a, float b) { return fmaxf(a,
 //
 // Block max (sglang #45451, Modifications / Accuracy Tests: "max").
 struct MaxScore {
+  static constexpr bool kWholeBlockUnroll = true;
   float m0 = -INFINITY, m1 = -INFINITY;
   float post = 1.f;  // exact power-of-two rescale of the raw dot products
   __device__ __forceinline__ explicit MaxScore(float post_scale) : post(post_scale) {}
@@ -212,6 +213,7 @@ struct MaxScore {
 // of a row in with one rescale and no branch (a masked value enters as -inf and
 // adds 2^-inf = 0).  lse = (m c + log2 sum) ln 2.
 struct LseScore {
+  static constexpr bool kWholeBlockUnroll = false;
   float m0 = -INFINITY, s0 = 0.f, m1 = -INFINITY, s1 = 0.f;
   float c;
   __device__ __forceinline__ explicit LseScore(float post_scale)
@@ -454,7 +456,10 @@ struct BlockScorer<kNvfp4> {
     const uint32_t th = (uint32_t)(t >> 1);
     // byte selectors {th, th, 2+th, 2+th}: duplicate the scale of group 2m + th
     const uint32_t sel = th | (th << 4) | ((2 + th) << 8) | ((2 + th) << 12);
-#pragma unroll 16  // whole block: measured 3-4% faster than two slices at a time
+    // the block max scores a whole block per loop (measured 3-4% faster than
+    // two slices at a time); the lse accumulator needs the registers
+    constexpr int kUnroll = Score::kWholeBlockUnroll ? 16 : 2;
+#pragma unroll kUnroll
     for (int nt = 0; nt < 16; ++nt) {
       // B operand: this lane's ldmatrix row address (token nt*8 + rr, chunk m)
       const int j = nt * 8 + rr;

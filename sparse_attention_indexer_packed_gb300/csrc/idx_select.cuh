@@ -118,7 +118,6 @@ struct Shared {
   uint32_t hist[256];
   unsigned long long sel[kCap];
   uint32_t red_min[NW], red_max[NW];
-  int wsum[NW];
   int count;
   uint32_t digit, need, bin;
 };
@@ -181,6 +180,9 @@ __device__ void row_select(const TopkArgs& a, int row, const RowPlan& pl, uint8_
     sh.red_min[warp] = kmin;
     sh.red_max[warp] = kmax;
   }
+  // the first radix pass's histogram and the gather's counter start at zero
+  for (int h = tid; h < 256; h += NT) sh.hist[h] = 0u;
+  if (tid == 0) sh.count = 0;
   __syncthreads();
   kmin = sh.red_min[0];
   kmax = sh.red_max[0];
@@ -200,11 +202,15 @@ __device__ void row_select(const TopkArgs& a, int row, const RowPlan& pl, uint8_
     int hi = 32 - __clz(kmin ^ kmax);  // bits [hi, 32) are common to all candidates
     fixed_mask = hi >= 32 ? 0u : (0xffffffffu << hi);
     fixed_val = kmax & fixed_mask;
+    bool first = true;
     while (hi > 0 && ksize > stop) {
       const int lo = max(hi - 8, 0);
       const uint32_t dmask = (1u << (hi - lo)) - 1u;
-      for (int h = tid; h < 256; h += NT) sh.hist[h] = 0u;
-      __syncthreads();
+      if (!first) {  // the previous pass's scan has read its histogram
+        for (int h = tid; h < 256; h += NT) sh.hist[h] = 0u;
+        __syncthreads();
+      }
+      first = false;
       for (int t = tid; t < ncand; t += NT) {
         const uint32_t k = keys[t];
         if ((k & fixed_mask) == fixed_val) atomicAdd(&sh.hist[(k >> lo) & dmask], 1u);
@@ -253,28 +259,24 @@ __device__ void row_select(const TopkArgs& a, int row, const RowPlan& pl, uint8_
   // to the exact threshold) the keys above it plus the `need` lowest ids equal
   // to it.  Either way each entry is then placed by its rank.
   const bool small = ksize <= (uint32_t)kCap;
-  int mine = 0;
-  for (int t = tid; t < ncand; t += NT) {
-    const uint32_t km = keys[t] & fixed_mask;
-    mine += (small ? (km >= fixed_val) : (km > fixed_val)) ? 1 : 0;
-  }
-  int incl = mine;  // inclusive prefix of the per-thread counts, in thread order
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sh.wsum[warp] = incl;
-  __syncthreads();
-  int base = incl - mine;
-  for (int w = 0; w < warp; ++w) base += sh.wsum[w];
-  if (tid == NT - 1) sh.count = base + mine;
-  for (int t = tid; t < ncand; t += NT) {
-    const uint32_t k = keys[t];
-    const uint32_t km = k & fixed_mask;
-    if (small ? (km >= fixed_val) : (km > fixed_val)) {
-      if (base < kCap) sel[base] = pack(k, fi + t);
-      ++base;
+  // each warp appends its entries at a shared counter (one atomic per warp and
+  // round); their order is irrelevant, the ranks place them
+  for (int t0 = 0; t0 < ncand; t0 += NT) {
+    const int t = t0 + tid;
+    uint32_t k = 0;
+    bool take = false;
+    if (t < ncand) {
+      k = keys[t];
+      const uint32_t km = k & fixed_mask;
+      take = small ? (km >= fixed_val) : (km > fixed_val);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (m) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sh.count, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const int at = base + __popc(m & ((1u << lane) - 1u));
+      if (take && at < kCap) sel[at] = pack(k, fi + t);
     }
   }
   __syncthreads();
@@ -294,7 +296,7 @@ __device__ void row_select(const TopkArgs& a, int row, const RowPlan& pl, uint8_
     }
     if (lane == 0) sh.count = b;
   }
-  __syncthreads();
+  if (!small) __syncthreads();
 
   // ---- place each entry by its rank (key desc, id asc); keep ranks < c ----
   const int n = min(sh.count, kCap);
