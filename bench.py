@@ -653,7 +653,8 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
     stage them: a step's inputs sit back to back in one pinned buffer (one copy
     in), its outputs in one device buffer (one copy out), and the copies run on a
     copy stream with two device buffer sets, so step k + 1's inputs are copied in
-    and step k's outputs copied out while the next step's kernels run.  Keys that
+    and step k's outputs copied out while the next step's kernels run; the
+    copies' events are waited for at the previous step's top-k launch.  Keys that
     fit in L2 are rotated over enough identical copies of the pool (at least
     twice L2 in all) that no step finds its keys in L2 from an earlier one."""
     s = batch.spec
@@ -691,14 +692,19 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
             d_in[i].copy_(h_in, non_blocking=True)
             ev_in[i].record(cs)
 
-    def compute(k, st):
+    def compute(k, st, last):
+        # The step's dependencies on the copy stream are hung on the previous
+        # step's top-k launch (idx_set_kernel_waits), not on this step's score
+        # launch, so the score kernel keeps its programmatic overlap with the
+        # step before it: step k + 1's inputs (copied after step k - 1's outputs
+        # on the copy stream) are waited for before step k's top-k; the first
+        # step of a run waits before its score kernel.
         i = k % 2
-        st.wait_event(ev_in[i])
-        if k >= 2:
-            st.wait_event(ev_out[i])           # step k - 2's outputs are out
         q, pt, sl, ln = vin[i][:4]
         qs = vin[i][4] if batch.q_scale is not None else None
         kp, ks = pools[k % npool]
+        idx.idx_set_kernel_waits(ev_in[i] if k == 0 else None,
+                                 None if last else ev_in[(k + 1) % 2])
         fn(q, qs, kp, ks, s.k_dtype, pt, sl, ln, s.packed_queries, s.gqa,
            s.init_blocks, s.local_blocks, topk, vout[i][0], vout[i][1], wsp, st)
         ev_used[i].record(st)
@@ -720,7 +726,7 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
         for k in range(n):
             if k + 1 < n:
                 copy_in(k + 1)
-            compute(k, st)
+            compute(k, st, k + 1 == n)
             copy_out(k)
         st.wait_event(ev_out[(n - 1) % 2])
 
@@ -771,8 +777,9 @@ def run_e2e(idx, batch, payload, scale, dev, stream, args):
             "note": "keys stay resident in the pool (a layer's index-K cache); q, page table, "
                     "slot ids and row lengths are copied in (one pinned staging buffer, one "
                     "copy), ids and scores copied out (one copy), on a copy stream that "
-                    "overlaps them with the neighbouring steps' kernels; the steps replayed "
-                    "from a CUDA graph of steps_per_graph steps",
+                    "overlaps them with the neighbouring steps' kernels (step k + 1's input "
+                    "copy is waited for at step k's top-k launch, idx_set_kernel_waits); the "
+                    "steps replayed from a CUDA graph of steps_per_graph steps",
             "steps_per_graph": G, "mode": mode}
 
 

@@ -286,6 +286,21 @@ IDX_API int idx_score_topk_perrow(const void* q, const float* q_scale, int q_dty
  * The events are used once and then forgotten. */
 IDX_API int idx_set_kernel_events(void* score_begin, void* score_end, void* topk_end);
 
+/* idx_set_kernel_waits — ordering for pipelined callers.  Arms, for the next
+ * idx_score_topk / _lse / _perrow / idx_score_local_blocks call on the calling
+ * host thread only, up to two cudaEvent_t (passed as void*, NULL to skip) that
+ * the call's stream waits for (cudaStreamWaitEvent): before_score before the
+ * score kernel is launched, before_topk before the top-k kernel is launched.
+ * The events are used once and then forgotten.  What it is for: the score
+ * kernel is launched as a programmatic dependent of the kernel before it and
+ * starts under it, but a wait placed right before it (a cross-stream event, a
+ * captured graph's join) makes it start only after that kernel has finished.
+ * A loop that copies step k + 1's inputs on another stream can hand that
+ * copy's event to step k's call as before_topk: step k + 1's score kernel reads
+ * its inputs only after step k's top-k has completed, which now comes after the
+ * copy, and keeps its overlap with step k.  Always returns IDX_OK. */
+IDX_API int idx_set_kernel_waits(void* before_score, void* before_topk);
+
 /*
  * idx_score_topk_noalloc — idx_score_topk for callers that cannot allocate device
  * memory.  (The pages have no counterpart: it is an addition of this library.)

@@ -66,6 +66,7 @@ _SIGNATURES = {
     "idx_score_topk_noalloc": (_I, [_P, _P, _I, _P, _P, _I, _I64, _P, _I, _I, _P, _P, _I, _I,
                                     _I, _I, _I, _I, _P, _P, _P]),
     "idx_set_kernel_events": (_I, [_P, _P, _P]),
+    "idx_set_kernel_waits": (_I, [_P, _P]),
     "idx_set_grid_limit": (_I, [_I]),
     "idx_workspace_errors": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "idx_noalloc_errors": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -274,6 +275,13 @@ def idx_set_kernel_events(score_begin=None, score_end=None, topk_end=None) -> No
     """Arm torch.cuda.Event objects (enable_timing=True) for the next score call."""
     h = [None if e is None else e.cuda_event for e in (score_begin, score_end, topk_end)]
     _check(lib().idx_set_kernel_events(*h), "idx_set_kernel_events")
+
+
+def idx_set_kernel_waits(before_score=None, before_topk=None) -> None:
+    """Arm torch.cuda.Event objects the next score call's stream waits for before
+    its score kernel / its top-k kernel (include/idx.h: idx_set_kernel_waits)."""
+    h = [None if e is None else e.cuda_event for e in (before_score, before_topk)]
+    _check(lib().idx_set_kernel_waits(*h), "idx_set_kernel_waits")
 
 
 def idx_score_topk_noalloc(q, q_scale, k_payload, k_scale, k_dtype, page_table, slot_ids,

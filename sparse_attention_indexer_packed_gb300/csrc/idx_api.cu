@@ -20,6 +20,7 @@ namespace {
 
 thread_local std::string g_last_error;
 thread_local cudaEvent_t g_ev[3] = {nullptr, nullptr, nullptr};
+thread_local cudaEvent_t g_wait[2] = {nullptr, nullptr};
 
 int fail(int status, const char* fmt, ...) {
   char buf[512];
@@ -300,6 +301,8 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   }
   cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
   g_ev[0] = g_ev[1] = g_ev[2] = nullptr;
+  const cudaEvent_t wait_score = g_wait[0], wait_topk = g_wait[1];
+  g_wait[0] = g_wait[1] = nullptr;
 
   idx::TopkArgs ta;
   ta.blockmax = sa.blockmax;
@@ -336,15 +339,21 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
 #else
   const bool fused = false;
 #endif
+  if (wait_score && (e = cudaStreamWaitEvent(st, wait_score, 0)) != cudaSuccess)
+    return cuda_fail(e, "waiting for the score kernel's event");
   if (ev[0] && (e = record_event(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
   e = wide ? idx::launch_wide(k_dtype, block_score, sa, map, qmap, st)
            : idx::launch_score(k_dtype, block_score, sa, map, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
   if (ev[1] && (e = record_event(ev[1], st)) != cudaSuccess) return cuda_fail(e, "event");
   if (fused) {
+    if (wait_topk && (e = cudaStreamWaitEvent(st, wait_topk, 0)) != cudaSuccess)
+      return cuda_fail(e, "waiting for the top-k kernel's event");
     if (ev[2] && (e = record_event(ev[2], st)) != cudaSuccess) return cuda_fail(e, "event");
     return IDX_OK;
   }
+  if (wait_topk && (e = cudaStreamWaitEvent(st, wait_topk, 0)) != cudaSuccess)
+    return cuda_fail(e, "waiting for the top-k kernel's event");
   e = idx::launch_topk(ta, st);
   if (e != cudaSuccess) {
     // the top-k kernel is what leaves the dynamic-schedule counter at zero and
@@ -515,6 +524,12 @@ int idx_set_kernel_events(void* score_begin, void* score_end, void* topk_end) {
   g_ev[0] = static_cast<cudaEvent_t>(score_begin);
   g_ev[1] = static_cast<cudaEvent_t>(score_end);
   g_ev[2] = static_cast<cudaEvent_t>(topk_end);
+  return IDX_OK;
+}
+
+int idx_set_kernel_waits(void* before_score, void* before_topk) {
+  g_wait[0] = static_cast<cudaEvent_t>(before_score);
+  g_wait[1] = static_cast<cudaEvent_t>(before_topk);
   return IDX_OK;
 }
 

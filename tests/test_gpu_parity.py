@@ -442,3 +442,61 @@ def test_wait_timeout_is_reported_and_the_context_survives(k_dtype, q_dtype, P, 
     assert good.flags == 0
     ref = oracle.index.index_step(**oracle_kwargs(b))
     _check_all_rows(b, good, ref)
+
+
+def test_kernel_waits_order_a_pipelined_step():
+    """idx_set_kernel_waits: inputs copied on another stream behind a long
+    kernel.  Waited for before the score kernel, or before the previous call's
+    top-k (the next call's score kernel reads its inputs only after that top-k),
+    the results equal the plain call's bit for bit; the inputs' buffers hold
+    zeros until the copies land, so a wait that is not honoured shows."""
+    import sparse_attention_indexer_packed_gb300 as idx
+    spec = workloads.small_spec("kw", 611, "bf16", "bf16", R=5, len_range=(2000, 12000), topk=24)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    ref = _gpu.run(b, planes=planes)
+    dev = "cuda"
+    s = b.spec
+    pt, sl, ln = b.page_table.to(dev), b.slot_ids.to(dev), b.row_lens.to(dev)
+    q_host = b.q.pin_memory()
+    side = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+
+    def out_bufs():
+        return (torch.full((b.R, b.M, s.topk), 77, dtype=torch.int32, device=dev),
+                torch.full((b.R, b.M, s.topk), 77.0, dtype=torch.float32, device=dev))
+
+    def call(q, ids, sc, ws):
+        idx.idx_score_topk(q, None, planes[0], planes[1], s.k_dtype, pt, sl, ln,
+                           s.packed_queries, s.gqa, s.init_blocks, s.local_blocks, s.topk,
+                           ids, sc, ws, main)
+
+    def staged_copy(q_dev):
+        ev = torch.cuda.Event()
+        side.wait_stream(main)                  # after the buffer's zero fill
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(20_000_000)       # ~10 ms of spinning before the copy
+            q_dev.copy_(q_host, non_blocking=True)
+            ev.record(side)
+        return ev
+
+    ws1 = idx.alloc_workspace(b.R, s.packed_queries, s.gqa, b.max_pages)
+    ws2 = idx.alloc_workspace(b.R, s.packed_queries, s.gqa, b.max_pages)
+    # before the score kernel
+    q1 = torch.zeros_like(b.q, device=dev)
+    ev1 = staged_copy(q1)
+    ids1, sc1 = out_bufs()
+    idx.idx_set_kernel_waits(ev1, None)
+    call(q1, ids1, sc1, ws1)
+    # before the previous call's top-k
+    q2 = torch.zeros_like(b.q, device=dev)
+    ev2 = staged_copy(q2)
+    ids0, sc0 = out_bufs()
+    idx.idx_set_kernel_waits(None, ev2)
+    call(b.q.to(dev), ids0, sc0, ws1)
+    ids2, sc2 = out_bufs()
+    call(q2, ids2, sc2, ws2)
+    torch.cuda.synchronize()
+    for ids, sc in [(ids1, sc1), (ids0, sc0), (ids2, sc2)]:
+        assert np.array_equal(ids.cpu().numpy(), ref.ids)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), ref.scores.view(np.uint32))
