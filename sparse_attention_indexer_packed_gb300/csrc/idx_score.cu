@@ -645,8 +645,10 @@ __device__ __forceinline__ void build_groups(const ScoreArgs& a, int* pre, int* 
   if (lane == 0) {
     pre[V] = run;
     // the last part of the blocks is handed out at run time, which evens out
-    // the CTAs' finish times: an eighth from ~600 blocks per CTA, a quarter
-    // from 64 (measured best on 16 x 131K bf16 / fp8 calls); NVFP4 calls
+    // the CTAs' finish times: an eighth from ~600 blocks per CTA, from 64 a
+    // quarter for bf16 and an eighth for fp8 (measured best on 16 x 131K
+    // calls: bf16 82.7 us a step against 84.3 with an eighth, fp8 52.9 against
+    // 53.6 with a quarter; all static: 87.2 / 56.8); NVFP4 calls
     // below 600 stay static, since a block from another request costs a
     // query-tile conversion there.  Only when a previous call left the
     // counter at zero (its tag says so).
@@ -654,7 +656,7 @@ __device__ __forceinline__ void build_groups(const ScoreArgs& a, int* pre, int* 
     int share = 0;  // 1 / share of the blocks is dynamic
     if (tag_ok) {
       if (run >= 600 * grid) share = 8;
-      else if (KF != kNvfp4 && run >= 64 * grid) share = 4;
+      else if (KF != kNvfp4 && run >= 64 * grid) share = KF == kFp8 ? 8 : 4;
     }
     ctl[0] = run;
     ctl[1] = share ? run - run / share : run;
