@@ -105,13 +105,9 @@ __device__ __forceinline__ void warp_place_sorted(const unsigned long long* list
 // kMinCtas = 8 caps registers at 32 so that eight rows share an SM (more than
 // six rows per SM: one wave instead of two); 0 (no minimum) leaves the
 // compiler the registers that keep a long row's loads in flight, measured
-// faster for a few hundred rows of ~1000 blocks.
-// kMinCtas = 8 caps registers at 32 so that eight rows share an SM (more than
-// six rows per SM: one wave instead of two); 0 (no minimum) leaves the
-// compiler the registers that keep a long row's loads in flight, measured
-// faster for a few hundred rows of ~1000 blocks.
-template <int kMinCtas>
-__global__ void __launch_bounds__(kThreads, kMinCtas) topk_kernel(const TopkArgs a) {
+// faster for a few hundred rows of ~1000 blocks.  NT is the row's threads.
+template <int kMinCtas, int NT>
+__global__ void __launch_bounds__(NT, kMinCtas) topk_kernel(const TopkArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int tid = threadIdx.x;
   // the next call's score kernel may become resident as soon as every row of
@@ -121,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) topk_kernel(const TopkArgs
   const int r = row / a.M;
   const RowPlan pl = row_plan(a, r, row - r * a.M);
   // pads need no block maxima: write them before waiting on the score kernel
-  sel::row_pads<kThreads>(a, row, pl, tid);
+  sel::row_pads<NT>(a, row, pl, tid);
   // launched as a programmatic dependent of the score kernel: wait for its
   // completion before touching the block maxima
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -130,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) topk_kernel(const TopkArgs
     *reinterpret_cast<volatile uint32_t*>(a.sched_counter) = 0u;
     *reinterpret_cast<volatile unsigned long long*>(a.sched_tag) = kSchedTag;
   }
-  sel::row_select<kThreads, false>(a, row, pl, smem_raw, tid);
+  sel::row_select<NT, false>(a, row, pl, smem_raw, tid);
 }
 
 // ---------------------------------------------------------------------------
@@ -429,21 +425,21 @@ __global__ void __launch_bounds__(32 * kMergeRowsPerCta) merge_kernel(const Merg
 
 }  // namespace
 
-template <int kMinCtas>
+template <int kMinCtas, int NT>
 cudaError_t launch_topk_cta(const TopkArgs& a, int rows, cudaStream_t stream) {
-  const size_t smem = sel::smem_bytes<kThreads>(a.nb_cap);
+  const size_t smem = sel::smem_bytes<NT>(a.nb_cap);
   // the limit is raised once per device to what the largest page table
   // (65536 pages: 32768 blocks) can need; each launch asks for its own size
   static std::atomic<unsigned long long> attr_done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = smem_limit_once(topk_kernel<kMinCtas>, (int)sel::smem_bytes<kThreads>(32768), dev,
+  e = smem_limit_once(topk_kernel<kMinCtas, NT>, (int)sel::smem_bytes<NT>(32768), dev,
                       attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)rows);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -451,7 +447,7 @@ cudaError_t launch_topk_cta(const TopkArgs& a, int rows, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_kernel<kMinCtas>, a);
+  e = cudaLaunchKernelEx(&cfg, topk_kernel<kMinCtas, NT>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -466,8 +462,11 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     if (a.nb_cap <= 128) return launch_topk_warp<4>(a, rows, stream);
     if (a.nb_cap <= 256) return launch_topk_warp<8>(a, rows, stream);
   }
-  if (rows > 6 * cached_sm_count(cur)) return launch_topk_cta<8>(a, rows, stream);
-  return launch_topk_cta<0>(a, rows, stream);
+  if (rows > 6 * cached_sm_count(cur)) return launch_topk_cta<8, kThreads>(a, rows, stream);
+  // at most two rows per SM: 512 threads a row (measured 0.6 us off a 16 x
+  // 131K bf16 step; more rows per SM were slower with them)
+  if (rows <= 2 * cached_sm_count(cur)) return launch_topk_cta<0, 2 * kThreads>(a, rows, stream);
+  return launch_topk_cta<0, kThreads>(a, rows, stream);
 }
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
