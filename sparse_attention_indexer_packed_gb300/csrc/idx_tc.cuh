@@ -94,6 +94,44 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// Whole-warp forms: every lane of a converged warp executes them with the same
+// (warp-uniform) operands and one lane, chosen by elect.sync (the same lane each
+// time in a converged warp), issues.  Issued this way the operands stay in
+// uniform registers; measured on sm_103a, an M = N = 128 bf16 MMA then issues
+// every ~87 cycles against ~100-120 from a single thread inside a lane branch,
+// and M = 128, N = 256 reaches the tensor cores' full rate.
+__device__ __forceinline__ void tc_mma_f16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f8_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Commit from the lane that issued the warp's MMAs (the same election).
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
+
 // Arrive (once) on the mbarrier when every tcgen05.mma this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {

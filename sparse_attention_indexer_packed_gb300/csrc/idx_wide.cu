@@ -549,7 +549,10 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
-    if (lane == 0) {
+    // The whole warp runs the loop with warp-uniform values; one elected lane
+    // issues each MMA and commit (tc_*_warp).  Every wait is taken by all lanes
+    // and its outcome agreed with a vote, so the warp stays converged.
+    {
       int prev_v = -1, nq = 0, i = 0, nt = 1;
       bool ok = true;
       int v = 0, b = 0;
@@ -558,8 +561,9 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         if (v != prev_v) {
           // stall test: the first wait goes to a barrier nothing completes
           const bool stall = a.stall_test && nq == 0;
-          if (!mbar_wait_bounded(stall ? sb + L::kCtlOff + 32 : L::qfull(sb), stall ? 0u : nq & 1,
-                                 a.wait_ns)) {
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_bounded(stall ? sb + L::kCtlOff + 32 : L::qfull(sb),
+                                            stall ? 0u : nq & 1, a.wait_ns))) {
             ok = false;
             break;
           }
@@ -571,14 +575,25 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         uint32_t opnd;
         if constexpr (KF == kNvfp4) {
           const int d = i % SD;
-          if (!mbar_wait_bounded(L::dfull(sb, d), (i / SD) & 1, a.wait_ns)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(L::dfull(sb, d), (i / SD) & 1, a.wait_ns))) {
+            ok = false;
+            break;
+          }
           opnd = sb + L::kDecOff + d * 32768;
         } else {
-          if (!mbar_wait_bounded(L::full(sb, s), (i / S) & 1, a.wait_ns)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(L::full(sb, s), (i / S) & 1, a.wait_ns))) {
+            ok = false;
+            break;
+          }
           opnd = sb + L::kStageOff + s * C::kStageBytes;
         }
         const int j = i % kUnits;
-        if (i >= kUnits && !mbar_wait_bounded(L::aempty(sb, j), ((i / kUnits) - 1) & 1, a.wait_ns)) { ok = false; break; }
+        if (i >= kUnits &&
+            !__all_sync(0xffffffffu,
+                        mbar_wait_bounded(L::aempty(sb, j), ((i / kUnits) - 1) & 1, a.wait_ns))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         // both tiles of the pair against the same staged keys
         for (int t = 0; t < nt; ++t) {
@@ -587,30 +602,30 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
           if (KF == kFp8) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc_mma_f8(d_tmem, desc_kmajor_sw128(qt + ks * 32), desc_kmajor_sw128(opnd + ks * 32),
-                        C::kIdesc, ks > 0 ? 1u : 0u);
+              tc_mma_f8_warp(d_tmem, desc_kmajor_sw128(qt + ks * 32),
+                             desc_kmajor_sw128(opnd + ks * 32), C::kIdesc, ks > 0 ? 1u : 0u);
           } else {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
-              tc_mma_f16(d_tmem, desc_kmajor_sw128(qt + off), desc_kmajor_sw128(opnd + off),
-                         C::kIdesc, ks > 0 ? 1u : 0u);
+              tc_mma_f16_warp(d_tmem, desc_kmajor_sw128(qt + off), desc_kmajor_sw128(opnd + off),
+                              C::kIdesc, ks > 0 ? 1u : 0u);
             }
           }
         }
-        if constexpr (KF == kNvfp4) tc_commit(L::dempty(sb, i % SD));
-        else tc_commit(L::empty(sb, s));
-        tc_commit(L::afull(sb, j));
+        if constexpr (KF == kNvfp4) tc_commit_warp(L::dempty(sb, i % SD));
+        else tc_commit_warp(L::empty(sb, s));
+        tc_commit_warp(L::afull(sb, j));
         int vn = v, bn = b;
         if (u + 1 < u1) wnext(gpre, V, vn, bn);
         else vn = -1;
-        if (vn != v) tc_commit(L::qempty(sb));  // last block of this pair
+        if (vn != v) tc_commit_warp(L::qempty(sb));  // last block of this pair
         v = vn;
         b = bn;
       }
-      if (!ok) atomicOr(cta_flags, kErrTimeout);
+      if (!ok && lane == 0) atomicOr(cta_flags, kErrTimeout);
       // every MMA issued has completed before TMEM is released
-      tc_commit(L::done(sb));
+      tc_commit_warp(L::done(sb));
       (void)mbar_wait_bounded(L::done(sb), 0, 200000000ull);
     }
     __syncwarp();
