@@ -191,6 +191,26 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// The three-input max of sm_100 and later: one instruction for two steps of a
+// running max (exact, so the order of the steps does not matter; finite inputs).
+__device__ __forceinline__ float fmax3_finite(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// {a.x * b.x, a.y * b.y}, each product rounded to nearest as by a plain fp32
+// multiply: one packed instruction for two.
+__device__ __forceinline__ float2 fmul2_rn(float2 a, float2 b) {
+  unsigned long long pa, pb, pd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(pd) : "l"(pa), "l"(pb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(pd));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

@@ -190,8 +190,8 @@ struct MaxScore {
       if (t0 < L1) m1 = fmax_finite(m1, v2);
       if (t0 + 1 < L1) m1 = fmax_finite(m1, v3);
     } else {
-      m0 = fmax_finite(m0, fmax_finite(v0, v1));
-      m1 = fmax_finite(m1, fmax_finite(v2, v3));
+      m0 = fmax3_finite(m0, v0, v1);
+      m1 = fmax3_finite(m1, v2, v3);
     }
   }
   __device__ __forceinline__ void reduce() {
@@ -439,8 +439,10 @@ struct BlockScorer<kFp8> {
       const int jt = nt * 8 + 2 * t;  // token of acc[0] within the block
       const float2 ks = *reinterpret_cast<const float2*>(scale_smem + jt);
       const int t0 = tbase + jt;
-      sc.template add<kMask>((acc[0] * qs0) * ks.x, (acc[1] * qs0) * ks.y, (acc[2] * qs1) * ks.x,
-                             (acc[3] * qs1) * ks.y, t0, L0, L1);
+      // (dot * q scale) * key scale, two scores per packed multiply
+      const float2 y0 = fmul2_rn(fmul2_rn(make_float2(acc[0], acc[1]), make_float2(qs0, qs0)), ks);
+      const float2 y1 = fmul2_rn(fmul2_rn(make_float2(acc[2], acc[3]), make_float2(qs1, qs1)), ks);
+      sc.template add<kMask>(y0.x, y0.y, y1.x, y1.y, t0, L0, L1);
     }
   }
 };

@@ -215,12 +215,20 @@ struct RowMax {
   template <bool kMask>
   __device__ __forceinline__ void add32(const float (&x)[32], int t0, int L) {
     float p = -INFINITY, q = -INFINITY;
+    if constexpr (!kMask) {
 #pragma unroll
-    for (int k = 0; k < 32; k += 2) {
-      if (!kMask || t0 + k < L) p = fmax_finite(p, x[k]);
-      if (!kMask || t0 + k + 1 < L) q = fmax_finite(q, x[k + 1]);
+      for (int k = 0; k < 32; k += 4) {
+        p = fmax3_finite(p, x[k], x[k + 1]);
+        q = fmax3_finite(q, x[k + 2], x[k + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        if (t0 + k < L) p = fmax_finite(p, x[k]);
+        if (t0 + k + 1 < L) q = fmax_finite(q, x[k + 1]);
+      }
     }
-    m = fmax_finite(m, fmax_finite(p, q));
+    m = fmax3_finite(m, p, q);
   }
   __device__ __forceinline__ float out() const { return m * post; }
 };
@@ -699,9 +707,17 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
             const int c0 = (h * kLd + hh) * 32;
             float x[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              x[k] = __uint_as_float(raw[hh][k]);
-              if (KF == kFp8) x[k] = (x[k] * qs) * ks[c0 + k];
+            for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(raw[hh][k]);
+            if constexpr (KF == kFp8) {
+              // (dot * q scale) * key scale, two columns per packed multiply
+              const float2 q2 = make_float2(qs, qs);
+#pragma unroll
+              for (int k = 0; k < 32; k += 2) {
+                const float2 kk = *reinterpret_cast<const float2*>(ks + c0 + k);
+                const float2 y = fmul2_rn(fmul2_rn(make_float2(x[k], x[k + 1]), q2), kk);
+                x[k] = y.x;
+                x[k + 1] = y.y;
+              }
             }
             if (whole) sc.template add32<false>(x, tbase + c0, Lrow);
             else sc.template add32<true>(x, tbase + c0, Lrow);
