@@ -299,6 +299,22 @@ def test_most_requests_per_call():
     _check_all_rows(b, out, ref)
 
 
+@pytest.mark.parametrize("length,seed", [(300_000, 511), (600_000, 512)])
+def test_long_rows_on_few_ctas(length, seed):
+    """One request of ~300K / ~600K tokens packing 2 draft rows x 2 heads, so
+    each row's selection runs on a 512-thread CTA and reads ~2300 / ~4700 block
+    scores with eight / sixteen loads in flight per thread.  Every row and block
+    score is checked against the oracle."""
+    spec = workloads.small_spec(f"long{length}", seed, "bf16", "bf16", R=1, P=2, G=2,
+                                len_range=(length - 1000, length), topk=64, local_blocks=4)
+    b = workloads.make_batch(spec)
+    out = _gpu.run(b)
+    assert out.flags == 0
+    ref = oracle.index.index_step(**oracle_kwargs(b))
+    _check_blockmax(b, out, ref)
+    _check_all_rows(b, out, ref)
+
+
 def test_topk_edge_values():
     """topk = init + local (no free choice), topk = 256, all scores equal."""
     spec = workloads.small_spec("e", 503, "bf16", "bf16", R=3, len_range=(1, 40000), topk=6)
