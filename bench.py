@@ -413,7 +413,38 @@ def time_step(idx, res, fn, dev, stream, args, ws_n, min_seconds):
         score_ms += [e[0].elapsed_time(e[1]) for e in evs]
         topk_ms += [e[1].elapsed_time(e[2]) for e in evs]
         step_ms += [e[0].elapsed_time(e[2]) for e in evs]
+    # isolated calls, the do_bench way: per rep the L2 flushed, then CUDA events
+    # around one step replayed from a one-step graph, so nothing of the step
+    # overlaps the one before it
+    iso_buf = (flush_buf if flush_buf is not None else
+               torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev))
+    if flush_buf is None:
+        g_one = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_one):
+            res.call(fn, dev)
+        g_one.replay()
+        torch.cuda.synchronize(dev)
+    else:
+        g_one = g_plain
+    iso_pairs = []
+    for _ in range(max(100, K)):
+        flush_l2(iso_buf)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g_one.replay()
+        b.record(stream)
+        iso_pairs.append((a, b))
+    torch.cuda.synchronize(dev)
+    iso_us = [a.elapsed_time(b) * 1e3 for a, b in iso_pairs]
+    del iso_buf
     return {
+        "isolated": {"median_us": round(max_over_ranks(statistics.median(iso_us), ws_n, dev), 3),
+                     "p10_us": round(percentile(iso_us, 0.1), 3),
+                     "p90_us": round(percentile(iso_us, 0.9), 3), "reps": len(iso_us),
+                     "how": "per rep: L2 flushed (256 MB written then read), then CUDA events "
+                            "around one step (score + top-k) replayed from a one-step CUDA "
+                            "graph; no overlap with the step before"},
         "value_us": value, "median_us": med, "p10_us": percentile(step_us, 0.1),
         "p90_us": percentile(step_us, 0.9), "samples": n_samples, "steps_per_sample": K,
         "timed_steps": n_samples * K, "timed_s": sum(elapsed(p) for p in samples) / 1e3,
@@ -477,7 +508,7 @@ def timing_record(t) -> dict:
             "p90_us": round(t["p90_us"], 3), "samples": t["samples"],
             "steps_per_sample": t["steps_per_sample"], "timed_steps": t["timed_steps"],
             "timed_s": round(t["timed_s"], 3), "steps_per_graph": t["steps_per_graph"],
-            "l2": t["l2"],
+            "l2": t["l2"], "isolated": t["isolated"],
             "how": "value = median over samples of K steps each (CUDA graph replays between "
                    "two CUDA events, samples back to back); score_us / topk_us: CUDA events "
                    "the library records around each kernel (external event nodes of a "
