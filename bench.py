@@ -503,6 +503,43 @@ def roofline(res, t, workload) -> dict:
     return out
 
 
+def time_store(idx, res, dev, stream, reps=20) -> dict:
+    """The NVFP4 quantize-store of the batch's keys (the write path, outside the
+    index step), timed on its own: every staged key quantised and written into
+    the pool planes.  Inputs are far larger than L2, so no flush."""
+    b = res.batch
+    src = b.staging.to(dev)
+    smap = b.slot_mapping.to(dev)
+    pool = (res.payload, res.scale)
+    for _ in range(3):
+        idx.idx_store_nvfp4(src, smap, pool, stream)
+    torch.cuda.synchronize(dev)
+    pairs = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        idx.idx_store_nvfp4(src, smap, pool, stream)
+        e.record(stream)
+        pairs.append((a, e))
+    torch.cuda.synchronize(dev)
+    us = [a.elapsed_time(e) * 1e3 for a, e in pairs]
+    keys = int(smap.numel())
+    live = int((smap >= 0).sum().item())
+    # per key: its 8-byte slot read; per stored key: 256 B of bf16 read, 64 B of
+    # codes and 8 B of scales written
+    nbytes = 8 * keys + live * (256 + 64 + 8)
+    med = statistics.median(us)
+    peak, peak_src = measured_peak()
+    del src, smap
+    achieved = nbytes / (med * 1e-6) / 1e9
+    return {"kernel": "store_nvfp4_kernel", "keys": keys, "us": round(med, 3),
+            "p10_us": round(percentile(us, 0.1), 3), "p90_us": round(percentile(us, 0.9), 3),
+            "reps": reps, "algorithmic_bytes": nbytes, "bound": "hbm",
+            "achieved": round(achieved, 1), "unit": "GB/s", "peak": peak,
+            "frac": round(achieved / peak, 4), "peak_source": peak_src}
+
+
 def timing_record(t) -> dict:
     return {"median_us": round(t["median_us"], 3), "p10_us": round(t["p10_us"], 3),
             "p90_us": round(t["p90_us"], 3), "samples": t["samples"],
@@ -577,10 +614,13 @@ def measure_extra(idx, name, args, dev, stream, ws_n, rank):
     t = time_step(idx, res, fn, dev, stream, args, ws_n, min_seconds=0.3)
     clocks = sampler.stop()
     e2e = run_e2e(idx, res.batch, res.payload, res.scale, dev, stream, args)
+    store = time_store(idx, res, dev, stream) if res.spec.k_dtype == "nvfp4" else None
     out = {"workload": name, "value": round(t["value_us"], 3), "unit": "us",
            "config": workload_config(res.spec, res.batch.R, args, ws_n, workload=name),
            "timing": timing_record(t), "roofline": roofline(res, t, name), "e2e": e2e,
            "clocks": clocks, "gpu_launches": 2 * t["timed_steps"]}
+    if store is not None:
+        out["store"] = store
     del res, t
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
@@ -621,6 +661,7 @@ def run_ours(args):
 
     # ---- end to end through the public API with host buffers ------------------
     e2e = run_e2e(idx, batch, res.payload, res.scale, dev, stream, args)
+    store = time_store(idx, res, dev, stream) if s.k_dtype == "nvfp4" else None
     rl = roofline(res, t, args.workload)
     ab = algorithmic_bytes(batch)
     value = t["value_us"]   # µs per step on each rank (replicas run concurrently)
@@ -647,6 +688,8 @@ def run_ours(args):
         "gpu_launches": 2 * t["timed_steps"],
         "clocks": clocks,
     }
+    if store is not None:
+        line["store"] = store
     del t["flush_buf"]
     if not args.no_extra:
         extras = [w for w in EXTRA_WORKLOADS if w != args.workload]

@@ -8,13 +8,26 @@
 //
 // Readings of the points the page leaves open: amax and amax/6 in fp32 with a
 // correctly rounded division; the scale rounds half-to-even and saturates at
-// 448; a zero scale writes all-zero codes; codes use x / scale with a correctly
-// rounded fp32 division; a negative value that rounds to zero keeps its sign.
+// 448; a zero scale writes all-zero codes; codes are those of the correctly
+// rounded fp32 quotient x / scale; a negative value that rounds to zero keeps
+// its sign.
+//
+// The codes come from the hardware e2m1 conversion (round to nearest, ties to
+// the even code, saturating at 6, the sign kept) of a quotient q2 that equals
+// x / s where that is on the e2m1 grid's midpoints and is within two ulps of it
+// elsewhere: q1 = x * r with r = 1 / s, the residual e = x - q1 * s (exact in
+// one fma), q2 = q1 + e * r (one correction step of a reciprocal-based
+// quotient, after Markstein, "IA-64 and Elementary Functions", 2000).  This is
+// enough: every midpoint t of the grid has at most three significant bits and
+// s at most four, so t * s is a bf16 value, and a bf16 x either equals t * s
+// (then the residual is exact and q2 = t) or lies a bf16 spacing away from it,
+// far beyond the quotient's error, on the same side as fl(x / s).
 //
 // One thread per (key, group of 16): eight threads cover a key, a warp four.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "idx_internal.cuh"
 
@@ -30,14 +43,28 @@ __device__ __forceinline__ float e4m3_magnitude(uint32_t b) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// e2m1 code of v: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the code with
-// a zero mantissa bit, saturating at 6; the sign bit follows v's sign.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  const float x = fabsf(v);
-  uint32_t c = (x > 0.25f) + (x >= 0.75f) + (x > 1.25f) + (x >= 1.75f) + (x > 2.5f) +
-               (x >= 3.5f) + (x > 5.0f);
-  if (signbit(v)) c |= 8u;
-  return c;
+__device__ __forceinline__ __nv_bfloat162 as_bf16x2(uint32_t u) {
+  __nv_bfloat162 v;
+  memcpy(&v, &u, sizeof(v));
+  return v;
+}
+
+// x / s on the e2m1 midpoints, within two ulps elsewhere (see above), with
+// x's sign (the fma steps would turn -0 into +0).
+__device__ __forceinline__ float grid_quotient(float x, float s, float r) {
+  const float q1 = x * r;
+  return copysignf(fmaf(fmaf(-q1, s, x), r, q1), x);
+}
+
+// Byte of two e2m1 codes: the code of lo in the low nibble, of hi in the high.
+__device__ __forceinline__ uint32_t e2m1x2_byte(float lo, float hi) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(d)
+      : "f"(hi), "f"(lo));
+  return d;
 }
 
 __global__ void __launch_bounds__(256) store_nvfp4_kernel(const uint16_t* __restrict__ src,
@@ -48,30 +75,33 @@ __global__ void __launch_bounds__(256) store_nvfp4_kernel(const uint16_t* __rest
   const int64_t tok = gid >> 3;
   const int grp = (int)(gid & 7);
   if (tok >= num_tokens) return;
+  // the key's bytes do not depend on its slot: both loads go out together
+  const uint4* p = reinterpret_cast<const uint4*>(src + tok * kDim + grp * 16);
   const int64_t row = __ldg(slot_mapping + tok);
+  const uint4 u0 = __ldcs(p), u1 = __ldcs(p + 1);
   if (row < 0 || row >= num_rows) return;
 
-  const uint4* p = reinterpret_cast<const uint4*>(src + tok * kDim + grp * 16);
-  const uint4 u0 = __ldg(p), u1 = __ldg(p + 1);
   const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-  float x[16];
-  float amax = 0.f;
+  // amax of the 16 magnitudes (a max is exact in any order)
+  __nv_bfloat162 m2 = as_bf16x2(w[0] & 0x7fff7fffu);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    x[2 * e] = __uint_as_float(w[e] << 16);
-    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    amax = fmaxf(amax, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
-  }
+  for (int e = 1; e < 8; ++e) m2 = __hmax2(m2, as_bf16x2(w[e] & 0x7fff7fffu));
+  const float amax = fmaxf(__low2float(m2), __high2float(m2));
   const float s_f = __fdiv_rn(amax, 6.0f);
   const uint32_t s_code =
       (uint32_t)__nv_cvt_float_to_fp8(s_f, __NV_SATFINITE, __NV_E4M3) & 0x7fu;
   const float s = e4m3_magnitude(s_code);
   uint32_t lo = 0, hi = 0;
   if (s > 0.f) {
+    const float r = __frcp_rn(s);
+    uint32_t byte[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) lo |= e2m1_code(__fdiv_rn(x[e], s)) << (4 * e);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) hi |= e2m1_code(__fdiv_rn(x[8 + e], s)) << (4 * e);
+    for (int e = 0; e < 8; ++e) {
+      const float x0 = __uint_as_float(w[e] << 16), x1 = __uint_as_float(w[e] & 0xffff0000u);
+      byte[e] = e2m1x2_byte(grid_quotient(x0, s, r), grid_quotient(x1, s, r));
+    }
+    lo = byte[0] | (byte[1] << 8) | (byte[2] << 16) | (byte[3] << 24);
+    hi = byte[4] | (byte[5] << 8) | (byte[6] << 16) | (byte[7] << 24);
   }
   *reinterpret_cast<uint2*>(payload + row * 64 + grp * 8) = make_uint2(lo, hi);
   scale[row * 8 + grp] = (uint8_t)s_code;

@@ -187,6 +187,56 @@ def test_nvfp4_store_golden_groups():
             assert P[row, 8 * g:8 * g + 8].tolist() == pay, (c, g, P[row].tolist())
 
 
+def _every_midpoint_groups():
+    """bf16 bit patterns [G, 16]: for every positive finite E4M3 scale s, groups
+    whose amax is 6 s (so amax / 6 = s exactly) holding each e2m1 midpoint t * s
+    (t in .25, .75, 1.25, 1.75, 2.5, 3.5, 5), its negation, its bf16 neighbours,
+    -0 and -6 s: every tie of the rounding at every scale."""
+    import oracle
+    groups = []
+    for code in range(1, 127):
+        s = float(oracle.formats.E4M3_TABLE[code])
+        bits = lambda v: int(np.array([v], np.float32).view(np.uint32)[0] >> 16)
+        vals = []
+        for t in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0):
+            b = bits(t * s)
+            assert np.array([t * s], np.float32)[0] == t * s
+            vals += [b, b | 0x8000, b - 1, b + 1]
+        six = bits(6 * s)
+        vals += [0x8000, six | 0x8000]                 # -0 and -6 s
+        for k in range(0, len(vals), 15):
+            g = [six] + vals[k:k + 15]
+            g += [0] * (16 - len(g))
+            groups.append(g)
+    return np.array(groups, dtype=np.uint16)
+
+
+def test_nvfp4_store_every_midpoint_of_every_scale():
+    """The store's codes at every tie of the e2m1 rounding, for all 126 scales,
+    bit for bit against the oracle's quantiser (ROCm/ATOM #2745, Summary:
+    half-to-even, saturating at 6; -0 and negatives that round to 0 keep the
+    sign)."""
+    import oracle
+    g = _every_midpoint_groups()
+    n_keys = -(-len(g) // 8)
+    bits = np.zeros((n_keys * 8, 16), dtype=np.uint16)
+    bits[:len(g)] = g
+    bits = bits.reshape(n_keys, 128)
+    want_pay, want_sc = oracle.formats.nvfp4_quantize(bits)
+    assert (want_sc.reshape(-1)[:len(g)] == np.repeat(np.arange(1, 127), 2)[:len(g)]).all()
+    src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    rows = torch.arange(n_keys, dtype=torch.int64) + 5
+    payload = torch.zeros((n_keys + 64, 64), dtype=torch.uint8, device="cuda")
+    scale = torch.zeros((n_keys + 64, 8), dtype=torch.uint8, device="cuda")
+    import sparse_attention_indexer_packed_gb300 as idx
+    idx.idx_store_nvfp4(src, rows.cuda(), (payload, scale))
+    P = payload.cpu().numpy()[5:5 + n_keys]
+    S = scale.cpu().numpy()[5:5 + n_keys]
+    assert np.array_equal(S, want_sc)
+    bad = np.argwhere(P != want_pay)
+    assert not len(bad), [(int(r), int(c), hex(P[r, c]), hex(want_pay[r, c])) for r, c in bad[:8]]
+
+
 # Unit roundoff of one fp32 addition that truncates instead of rounding (the
 # worst a tensor core's accumulation may do): 2^-23.
 _U_TRUNC = 2.0 ** -23
