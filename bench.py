@@ -46,6 +46,7 @@ L2_BYTES = 129 * 1024 * 1024
 L2_FLUSH_BYTES = 256 * 1024 * 1024
 SCORE_SOURCES = ["idx_score.cu", "idx_ptx.cuh", "idx_internal.cuh"]
 WIDE_SOURCES = ["idx_wide.cu", "idx_tc.cuh", "idx_ptx.cuh", "idx_internal.cuh"]
+STORE_SOURCES = ["idx_store.cu", "idx_internal.cuh"]
 
 
 def is_wide(spec) -> bool:
@@ -85,11 +86,11 @@ def code_only(text: str) -> str:
     return "".join(out).strip()
 
 
-def kernel_sha(wide: bool = False) -> str:
+def kernel_sha(wide: bool = False, sources=None) -> str:
     """Hash of the kernel sources as the compiler sees them (comments and
     layout left out); `profiles/traffic.json` holds DRAM counters per hash."""
     h = hashlib.sha256()
-    for f in (WIDE_SOURCES if wide else SCORE_SOURCES):
+    for f in (sources or (WIDE_SOURCES if wide else SCORE_SOURCES)):
         with open(os.path.join(ROOT, "sparse_attention_indexer_packed_gb300", "csrc", f),
                   encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode())
@@ -533,7 +534,15 @@ def time_store(idx, res, dev, stream, reps=20) -> dict:
     peak, peak_src = measured_peak()
     del src, smap
     achieved = nbytes / (med * 1e-6) / 1e9
-    return {"kernel": "store_nvfp4_kernel", "keys": keys, "us": round(med, 3),
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            tr = json.load(fh).get(res.spec.name + ":store")
+        if tr and tr.get("kernel_sha") == kernel_sha(sources=STORE_SOURCES):
+            traffic = tr["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return {"kernel": "store_nvfp4_kernel", "keys": keys, "us": round(med, 3), "traffic": traffic,
             "p10_us": round(percentile(us, 0.1), 3), "p90_us": round(percentile(us, 0.9), 3),
             "reps": reps, "algorithmic_bytes": nbytes, "bound": "hbm",
             "achieved": round(achieved, 1), "unit": "GB/s", "peak": peak,

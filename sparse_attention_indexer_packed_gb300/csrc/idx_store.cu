@@ -67,21 +67,9 @@ __device__ __forceinline__ uint32_t e2m1x2_byte(float lo, float hi) {
   return d;
 }
 
-__global__ void __launch_bounds__(256) store_nvfp4_kernel(const uint16_t* __restrict__ src,
-                                                          const int64_t* __restrict__ slot_mapping,
-                                                          int64_t num_tokens, uint8_t* payload,
-                                                          uint8_t* scale, int64_t num_rows) {
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t tok = gid >> 3;
-  const int grp = (int)(gid & 7);
-  if (tok >= num_tokens) return;
-  // the key's bytes do not depend on its slot: both loads go out together
-  const uint4* p = reinterpret_cast<const uint4*>(src + tok * kDim + grp * 16);
-  const int64_t row = __ldg(slot_mapping + tok);
-  const uint4 u0 = __ldcs(p), u1 = __ldcs(p + 1);
-  if (row < 0 || row >= num_rows) return;
-
-  const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+// Quantise one group (its 16 bf16 values in w) and write it.
+__device__ __forceinline__ void store_group(const uint32_t (&w)[8], int64_t row, int grp,
+                                            uint8_t* payload, uint8_t* scale) {
   // amax of the 16 magnitudes (a max is exact in any order)
   __nv_bfloat162 m2 = as_bf16x2(w[0] & 0x7fff7fffu);
 #pragma unroll
@@ -107,14 +95,48 @@ __global__ void __launch_bounds__(256) store_nvfp4_kernel(const uint16_t* __rest
   scale[row * 8 + grp] = (uint8_t)s_code;
 }
 
+// Each thread quantises kGroups groups, blockDim apart (each load instruction
+// of a warp covers 1 KB of consecutive keys); all their loads go out before
+// any of them is used.
+constexpr int kGroups = 2;
+
+__global__ void __launch_bounds__(256) store_nvfp4_kernel(const uint16_t* __restrict__ src,
+                                                          const int64_t* __restrict__ slot_mapping,
+                                                          int64_t num_tokens, uint8_t* payload,
+                                                          uint8_t* scale, int64_t num_rows) {
+  const int64_t base = (int64_t)blockIdx.x * blockDim.x * kGroups + threadIdx.x;
+  uint4 u[kGroups][2];
+  int64_t row[kGroups];
+#pragma unroll
+  for (int j = 0; j < kGroups; ++j) {
+    const int64_t gid = base + (int64_t)j * blockDim.x;
+    const int64_t tok = gid >> 3;
+    row[j] = -1;
+    if (tok < num_tokens) {
+      // the key's bytes do not depend on its slot: the loads go out together
+      const uint4* p = reinterpret_cast<const uint4*>(src + tok * kDim + (gid & 7) * 16);
+      row[j] = __ldg(slot_mapping + tok);
+      u[j][0] = __ldcs(p);
+      u[j][1] = __ldcs(p + 1);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kGroups; ++j) {
+    if (row[j] < 0 || row[j] >= num_rows) continue;
+    const uint32_t w[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
+                           u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+    store_group(w, row[j], (int)((base + (int64_t)j * blockDim.x) & 7), payload, scale);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_store_nvfp4(const uint16_t* src, const int64_t* slot_mapping, int64_t num_tokens,
                                uint8_t* payload, uint8_t* scale, int64_t num_rows,
                                cudaStream_t stream) {
   if (num_tokens <= 0) return cudaSuccess;
-  const int64_t threads = num_tokens * 8;
-  const int64_t blocks = (threads + 255) / 256;
+  const int64_t groups = num_tokens * 8;
+  const int64_t blocks = (groups + 256 * kGroups - 1) / (256 * kGroups);
   store_nvfp4_kernel<<<(unsigned)blocks, 256, 0, stream>>>(src, slot_mapping, num_tokens, payload,
                                                          scale, num_rows);
   return cudaGetLastError();

@@ -2,10 +2,12 @@
 
 The store kernel quantises a bf16 value v with an E4M3 scale s to the e2m1 code
 of q = fl(v / s) (ATOM #2745, Summary, "Store": codes of x / scale, rounded
-half-to-even, saturating at 6).  Instead of dividing it compares |v| with the
-products t * s of the e2m1 grid's midpoints t, arguing that t * s is exact and
-itself a bf16 value, so the rounding of the quotient can never cross it.  This
-test checks that equivalence for every finite bf16 magnitude against every
+half-to-even, saturating at 6) without a correctly rounded division.  Its
+argument: each product t * s of an e2m1 midpoint t and a scale is exact and
+itself a bf16 value, so a bf16 v is either exactly at t * s or a bf16 spacing
+away from it, and the rounding of the quotient can never carry it across t.
+This test checks the consequence, that comparing |v| with t * s decides every
+midpoint comparison of fl(v / s), for every finite bf16 magnitude against every
 positive finite E4M3 scale, with numpy's IEEE fp32 division as the reference.
 """
 import numpy as np
