@@ -277,18 +277,23 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // f16 query tile for NVFP4 keys: row i of the tile (one thread) is rescaled by
-// 2^qexp so its largest magnitude lies in [2^14, 2^15) and stored as f16 (when
-// `write`); every element within 2^-24 of that maximum is exact.  Returns 2^-qexp.
-__device__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i, int base_row,
-                               int nrows, bool write) {
+// 2^qexp so its largest magnitude lies in [2^14, 2^15) and stored as f16;
+// every element within 2^-24 of that maximum is exact.  The row is read in two
+// halves of eight loads in flight each (for its maximum, then again for the
+// conversion, from L1 or L2).  Returns 2^-qexp.
+__device__ __forceinline__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i,
+                                               int base_row, int nrows) {
   const bool valid = i < nrows;
   const uint4* src = reinterpret_cast<const uint4*>(a.q + (size_t)(base_row + i) * 256);
   float amax = 0.f;
-  if (valid) {
-#pragma unroll 4
-    for (int c = 0; c < 16; ++c) {
-      const uint4 u = __ldg(src + c);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint4 u[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) u[c] = valid ? __ldg(src + 8 * h + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         amax = fmaxf(amax, fabsf(__uint_as_float(w[e] << 16)));
@@ -300,21 +305,23 @@ __device__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i, int ba
   if (amax > 0.f) qexp = 14 - (((__float_as_uint(amax) >> 23) & 0xff) - 127);
   qexp = max(-100, min(100, qexp));
   const float up = ldexpf(1.f, qexp);
-  if (!write) return ldexpf(1.f, -qexp);
-#pragma unroll 4
-  for (int c = 0; c < 16; ++c) {
-    uint32_t o[4] = {0u, 0u, 0u, 0u};
-    if (valid) {
-      const uint4 u = __ldg(src + c);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint4 u[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) u[c] = valid ? __ldg(src + 8 * h + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+      uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        __half2 h = __floats2half2_rn(__uint_as_float(w[e] << 16) * up,
-                                      __uint_as_float(w[e] & 0xffff0000u) * up);
-        o[e] = *reinterpret_cast<uint32_t*>(&h);
+        __half2 hh = __floats2half2_rn(__uint_as_float(w[e] << 16) * up,
+                                       __uint_as_float(w[e] & 0xffff0000u) * up);
+        o[e] = *reinterpret_cast<uint32_t*>(&hh);
       }
+      st_shared_v4(sw128_chunk(qtile, i, 8 * h + c), o[0], o[1], o[2], o[3]);
     }
-    st_shared_v4(sw128_chunk(qtile, i, c), o[0], o[1], o[2], o[3]);
   }
   return ldexpf(1.f, -qexp);
 }
@@ -666,13 +673,24 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         if (KF == kFp8) qs = live ? __ldg(a.q_scale + out_row) : 0.f;
         if (KF == kNvfp4) {
           // each group writes its own f16 query tile once every MMA of the
-          // previous pair has completed
+          // previous pair has completed (its rows from L2 when the previous
+          // switch prefetched them)
           if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1, a.wait_ns)) ok = false;
           if (!__all_sync(0xffffffffu, ok)) break;
-          if (mine) post = convert_q_row(a, qtile + eg * C::kQBytes, ti, r * a.M + row0, nrows, true);
+          if (mine) post = convert_q_row(a, qtile + eg * C::kQBytes, ti, r * a.M + row0, nrows);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) mbar_arrive(L::qfull(sb));
+          // the next pair this CTA reaches: its query rows into L2 now, so the
+          // next switch does not wait on HBM for them
+          int vn = v + 1;
+          while (vn < V && gpre[vn + 1] == gpre[vn]) ++vn;
+          if (vn < V && gpre[vn] < u1) {
+            const int rn = vn / TP;
+            const int tn = 2 * (vn - rn * TP) + eg;
+            if (tn < a.tiles && ti < min(kWRows, a.M - tn * kWRows))
+              bulk_prefetch_l2(a.q + (size_t)(rn * a.M + tn * kWRows + ti) * 256, 256);
+          }
         }
         ++nq;
         prev_v = v;
