@@ -123,7 +123,10 @@ IDX_API int idx_store_nvfp4(const void* src_bf16, const int64_t* slot_mapping, i
  * idx_score_topk_workspace_bytes — device scratch idx_score_topk needs: a header of
  * IDX_WORKSPACE_HEADER_BYTES (device error flags) plus one fp32 block score per
  * (request, packed row, block): num_requests * packed_queries * gqa *
- * ceil(max_pages / 2) floats.
+ * ceil(max_pages / 2) floats.  When packed_queries * gqa > IDX_MAX_PACKED_ROWS
+ * (the 128-row tensor-core path) it adds, from the next 256-byte boundary, 260
+ * bytes per packed row: the rows of q converted once per call to f16 (NVFP4
+ * keys), and their scales.
  */
 IDX_API size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queries, int gqa,
                                       int max_pages);

@@ -294,9 +294,20 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   sa.shard = shard ? 1 : 0;
   sa.wait_ns = idx::wait_limit_ns();
   sa.stall_test = idx::stall_test();
+  sa.q16 = nullptr;
+  sa.qpost = nullptr;
   CUtensorMap qmap = map;
   if (wide && k_dtype != IDX_NVFP4) {
     rc = make_q_map(q_dtype, q, (int64_t)R * P * G, &qmap);
+    if (rc != IDX_OK) return rc;
+  } else if (wide) {
+    // NVFP4 keys: the query rows are converted to f16 once per call into the
+    // workspace (a small kernel before the score kernel), and the tiles load
+    // from there like bf16 ones (TMA copies bits: the bf16 map describes them)
+    const long long rows = (long long)R * P * G;
+    sa.q16 = reinterpret_cast<uint16_t*>(ws + idx::ws_q16_offset(rows, max_pages));
+    sa.qpost = reinterpret_cast<float*>(ws + idx::ws_q16_offset(rows, max_pages) + rows * 256);
+    rc = make_q_map(IDX_BF16, sa.q16, rows, &qmap);
     if (rc != IDX_OK) return rc;
   }
   cudaEvent_t ev[3] = {g_ev[0], g_ev[1], g_ev[2]};
@@ -342,6 +353,8 @@ int score_topk_impl(bool perrow, int block_score, int block_begin, const void* q
   if (wait_score && (e = cudaStreamWaitEvent(st, wait_score, 0)) != cudaSuccess)
     return cuda_fail(e, "waiting for the score kernel's event");
   if (ev[0] && (e = record_event(ev[0], st)) != cudaSuccess) return cuda_fail(e, "event");
+  if (sa.q16 && (e = idx::launch_q16(sa, st)) != cudaSuccess)
+    return cuda_fail(e, "launching the query conversion kernel");
   e = wide ? idx::launch_wide(k_dtype, block_score, sa, map, qmap, st)
            : idx::launch_score(k_dtype, block_score, sa, map, st);
   if (e != cudaSuccess) return cuda_fail(e, "launching the score kernel");
@@ -461,9 +474,10 @@ int idx_store_nvfp4(const void* src_bf16, const int64_t* slot_mapping, int64_t n
 size_t idx_score_topk_workspace_bytes(int num_requests, int packed_queries, int gqa,
                                       int max_pages) {
   if (num_requests < 0 || packed_queries < 1 || gqa < 1 || max_pages < 1) return 0;
-  const size_t nb_cap = (size_t)(max_pages + 1) / 2;
-  return IDX_WORKSPACE_HEADER_BYTES +
-         (size_t)num_requests * packed_queries * gqa * nb_cap * sizeof(float);
+  const long long rows = (long long)num_requests * packed_queries * gqa;
+  if ((long long)packed_queries * gqa > IDX_MAX_PACKED_ROWS)
+    return idx::ws_q16_offset(rows, max_pages) + idx::ws_wide_bytes(rows);
+  return IDX_WORKSPACE_HEADER_BYTES + idx::ws_blockmax_bytes(rows, max_pages);
 }
 
 int idx_score_topk(const void* q, const float* q_scale, int q_dtype, const void* k_payload,

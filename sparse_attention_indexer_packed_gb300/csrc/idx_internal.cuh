@@ -66,6 +66,17 @@ struct TopkArgs {
 
 // Arguments of one scoring pass.  A "group" is the set of tile rows that share
 // one read of the keys: a whole request when packed, one draft row when per-row.
+// Workspace layout: the header, the block scores, and for the wide path (more
+// than 16 packed rows) the f16 query rows and their scales from the next
+// 256-byte boundary.
+inline size_t ws_blockmax_bytes(long long rows, int max_pages) {
+  return (size_t)rows * (size_t)((max_pages + 1) / 2) * sizeof(float);
+}
+inline size_t ws_q16_offset(long long rows, int max_pages) {
+  return (kHeaderBytes + ws_blockmax_bytes(rows, max_pages) + 255) & ~(size_t)255;
+}
+inline size_t ws_wide_bytes(long long rows) { return (size_t)rows * (256 + sizeof(float)); }
+
 struct ScoreArgs {
   const uint8_t* q;            // [R][P][G][128] bf16 or e4m3
   const float* q_scale;        // [R][P*G] (e4m3 q) or nullptr
@@ -74,6 +85,8 @@ struct ScoreArgs {
   const int32_t* slot_ids;     // [R]
   const int32_t* row_lens;     // [R][P]
   float* blockmax;             // [R*P*G][nb_cap]
+  uint16_t* q16;               // wide path, NVFP4 keys: f16 query rows [R*P*G][128]
+  float* qpost;                // and the factor undoing each row's power-of-two scale
   uint8_t* err_bytes;          // one flag byte per CTA
   uint32_t* err_count;         // CTAs that wrote a flag byte
   uint32_t* sched_counter;     // dynamic-schedule block counter (zero at entry)
@@ -179,7 +192,11 @@ int grid_limit();
 cudaError_t launch_score(int key_format, int block_score, const ScoreArgs& args,
                          const CUtensorMap& payload_map, cudaStream_t stream);
 // Requests of more than 16 packed rows: 128-row tiles on tcgen05 (q_map: the
-// query rows [R*M][128] as bf16 or e4m3; unused for NVFP4 keys).
+// query rows [R*M][128] as bf16 or e4m3, or for NVFP4 keys the f16 rows
+// launch_q16 writes to args.q16).
+// Wide path with NVFP4 keys: the query rows to f16 (args.q16, args.qpost),
+// launched before the wide kernel.
+cudaError_t launch_q16(const ScoreArgs& args, cudaStream_t stream);
 cudaError_t launch_wide(int key_format, int block_score, const ScoreArgs& args,
                         const CUtensorMap& payload_map, const CUtensorMap& q_map,
                         cudaStream_t stream);

@@ -276,54 +276,51 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// f16 query tile for NVFP4 keys: row i of the tile (one thread) is rescaled by
-// 2^qexp so its largest magnitude lies in [2^14, 2^15) and stored as f16;
-// every element within 2^-24 of that maximum is exact.  The row is read in two
-// halves of eight loads in flight each (for its maximum, then again for the
-// conversion, from L1 or L2).  Returns 2^-qexp.
-__device__ __forceinline__ float convert_q_row(const ScoreArgs& a, uint32_t qtile, int i,
-                                               int base_row, int nrows) {
-  const bool valid = i < nrows;
-  const uint4* src = reinterpret_cast<const uint4*>(a.q + (size_t)(base_row + i) * 256);
+// f16 query rows for NVFP4 keys (the MMA takes f16 on both sides, and the
+// decoded keys are exact in f16): row i is rescaled by 2^qexp so its largest
+// magnitude lies in [2^14, 2^15) and stored as f16, every element within 2^-24
+// of that maximum exactly; qpost[i] = 2^-qexp undoes it on the scores.  One
+// thread a row, all its loads in flight together; run once per call before the
+// score kernel, which loads the f16 tiles by TMA.
+__global__ void __launch_bounds__(128) q16_kernel(const ScoreArgs a) {
+  // the score kernel may be scheduled at once; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the query rows may be written by the work before this call
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= (long long)a.R * a.M) return;
+  const uint4* src = reinterpret_cast<const uint4*>(a.q + row * 256);
+  uint4 u[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) u[c] = __ldg(src + c);
   float amax = 0.f;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint4 u[8];
+  for (int c = 0; c < 16; ++c) {
+    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
-    for (int c = 0; c < 8; ++c) u[c] = valid ? __ldg(src + 8 * h + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[e] << 16)));
-        amax = fmaxf(amax, fabsf(__uint_as_float(w[e] & 0xffff0000u)));
-      }
+    for (int e = 0; e < 4; ++e) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[e] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[e] & 0xffff0000u)));
     }
   }
   int qexp = 0;
   if (amax > 0.f) qexp = 14 - (((__float_as_uint(amax) >> 23) & 0xff) - 127);
   qexp = max(-100, min(100, qexp));
   const float up = ldexpf(1.f, qexp);
+  uint4* dst = reinterpret_cast<uint4*>(a.q16 + row * 128);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint4 u[8];
+  for (int c = 0; c < 16; ++c) {
+    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+    uint32_t o[4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) u[c] = valid ? __ldg(src + 8 * h + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __half2 hh = __floats2half2_rn(__uint_as_float(w[e] << 16) * up,
-                                       __uint_as_float(w[e] & 0xffff0000u) * up);
-        o[e] = *reinterpret_cast<uint32_t*>(&hh);
-      }
-      st_shared_v4(sw128_chunk(qtile, i, 8 * h + c), o[0], o[1], o[2], o[3]);
+    for (int e = 0; e < 4; ++e) {
+      __half2 hh = __floats2half2_rn(__uint_as_float(w[e] << 16) * up,
+                                     __uint_as_float(w[e] & 0xffff0000u) * up);
+      o[e] = *reinterpret_cast<uint32_t*>(&hh);
     }
+    dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  return ldexpf(1.f, -qexp);
+  a.qpost[row] = ldexpf(1.f, -qexp);
 }
 
 // Decode token n (0..127) of a raw NVFP4 stage into the f16 operand tile.
@@ -399,13 +396,13 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       mbar_init(L::afull(sb, j), 1);
       mbar_init(L::aempty(sb, j), 8);  // both epilogue groups, every block
     }
-    mbar_init(L::qfull(sb), KF == kNvfp4 ? 8 : 1);
+    mbar_init(L::qfull(sb), 1);
     mbar_init(L::qempty(sb), 1);
     mbar_init(L::done(sb), 1);
     mbar_init(sb + L::kCtlOff + 32, 1);  // the stall test's barrier
     fence_barrier_init();
     prefetch_tensormap(&kmap);
-    if (KF != kNvfp4) prefetch_tensormap(&qmap);
+    prefetch_tensormap(&qmap);
   }
   if (warp == 1) {
     tmem_alloc(sb + L::kCtlOff + 4, kTmemCols);
@@ -500,7 +497,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       const int p0 = __shfl_sync(0xffffffffu, wpg, 2 * k);
       const int p1 = __shfl_sync(0xffffffffu, wpg, 2 * k + 1);
       if (v != prev_v) {
-        if (KF != kNvfp4 && lane == 0) {
+        if (lane == 0) {
           // the previous pair's MMAs must be done with the query tiles
           if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1, a.wait_ns)) ok = false;
           if (ok) {
@@ -511,7 +508,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
             for (int t = 0; t < nt; ++t) {
               const int base_row = r * a.M + (tile0 + t) * kWRows;
               const uint32_t qt = qtile + t * C::kQBytes;
-              if (KF == kBf16) {
+              if (KF != kFp8) {  // bf16 rows, or the f16 rows made for NVFP4 keys
                 tma_load_2d(qt, &qmap, 0, base_row, L::qfull(sb));
                 tma_load_2d(qt + 16384, &qmap, 64, base_row, L::qfull(sb));
               } else {
@@ -560,7 +557,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       // when another role gave up early (instant when they were all consumed)
       for (int k = max(0, i - S); k < i; ++k)
         (void)mbar_wait_bounded(L::full(sb, k % S), (k / S) & 1, 200000000ull);
-      if (KF != kNvfp4 && nq > 0) (void)mbar_wait_bounded(L::qfull(sb), (nq - 1) & 1, 200000000ull);
+      if (nq > 0) (void)mbar_wait_bounded(L::qfull(sb), (nq - 1) & 1, 200000000ull);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -671,27 +668,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         out_row = live ? r * a.M + row0 + ti : -1;
         Lrow = live ? min(__ldg(a.row_lens + r * a.P + (row0 + ti) / a.G), a.max_pages * kPage) : 0;
         if (KF == kFp8) qs = live ? __ldg(a.q_scale + out_row) : 0.f;
-        if (KF == kNvfp4) {
-          // each group writes its own f16 query tile once every MMA of the
-          // previous pair has completed (its rows from L2 when the previous
-          // switch prefetched them)
-          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1, a.wait_ns)) ok = false;
-          if (!__all_sync(0xffffffffu, ok)) break;
-          if (mine) post = convert_q_row(a, qtile + eg * C::kQBytes, ti, r * a.M + row0, nrows);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(L::qfull(sb));
-          // the next pair this CTA reaches: its query rows into L2 now, so the
-          // next switch does not wait on HBM for them
-          int vn = v + 1;
-          while (vn < V && gpre[vn + 1] == gpre[vn]) ++vn;
-          if (vn < V && gpre[vn] < u1) {
-            const int rn = vn / TP;
-            const int tn = 2 * (vn - rn * TP) + eg;
-            if (tn < a.tiles && ti < min(kWRows, a.M - tn * kWRows))
-              bulk_prefetch_l2(a.q + (size_t)(rn * a.M + tn * kWRows + ti) * 256, 256);
-          }
-        }
+        if (KF == kNvfp4) post = live ? __ldg(a.qpost + out_row) : 1.f;
         ++nq;
         prev_v = v;
       }
@@ -784,6 +761,18 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     if (blockIdx.x == 0) *a.err_count = gridDim.x;
   }
 }
+
+}  // namespace
+
+cudaError_t launch_q16(const ScoreArgs& a, cudaStream_t stream) {
+  const long long rows = (long long)a.R * a.M;
+  if (rows <= 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(q16_kernel, (int)((rows + 127) / 128), 128, 0, stream, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+namespace {
 
 template <int KF, class RowScore>
 cudaError_t launch_wide_kf(const ScoreArgs& a, const CUtensorMap& kmap, const CUtensorMap& qmap,

@@ -43,6 +43,12 @@ def test_workspace_bytes(L):
     assert idx.idx_score_topk_workspace_bytes(16, 4, 4, 2048) == 1024 + 16 * 16 * 1024 * 4
     assert idx.idx_score_topk_workspace_bytes(1, 1, 1, 3) == 1024 + 2 * 4
     assert idx.idx_score_topk_workspace_bytes(0, 4, 4, 10) == 1024
+    # more than 16 packed rows: f16 query rows (256 B) and a scale (4 B) a row,
+    # from the 256-byte boundary after the block scores
+    rows, blocks = 4 * 512 * 4, 256
+    after = (1024 + rows * blocks * 4 + 255) // 256 * 256
+    assert idx.idx_score_topk_workspace_bytes(4, 512, 4, 512) == after + rows * 260
+    assert idx.idx_score_topk_workspace_bytes(1, 17, 1, 3) == (1024 + 17 * 2 * 4 + 255) // 256 * 256 + 17 * 260
 
 
 FAKE = 0x10000  # a non-NULL, 256-aligned value; every case below fails validation first
