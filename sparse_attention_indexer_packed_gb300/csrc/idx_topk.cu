@@ -45,11 +45,11 @@ using sel::RowPlan;
 constexpr int kThreads = 256;
 constexpr int kMaxWorld = 8;  // context shards a merge accepts
 
-// Descending bitonic sort of 32 E 64-bit values held by one warp, element
-// e = lane + 32 h in x[h] (E a power of two).  Partners closer than 32 are
-// exchanged by shuffles, farther ones inside the lane's registers.
-template <int E>
-__device__ __forceinline__ void warp_sort_desc(unsigned long long (&x)[E], int lane) {
+// Descending bitonic sort of 32 E values (32- or 64-bit) held by one warp,
+// element e = lane + 32 h in x[h] (E a power of two).  Partners closer than 32
+// are exchanged by shuffles, farther ones inside the lane's registers.
+template <int E, class T>
+__device__ __forceinline__ void warp_sort_desc(T (&x)[E], int lane) {
 #pragma unroll
   for (int k = 2; k <= 32 * E; k <<= 1) {
 #pragma unroll
@@ -61,7 +61,7 @@ __device__ __forceinline__ void warp_sort_desc(unsigned long long (&x)[E], int l
           if ((h & hj) == 0) {
             // pair (e, e + j), e = lane + 32 h; (e & k) depends on h alone
             const bool desc = ((32 * h) & k) == 0;
-            const unsigned long long a = x[h], b = x[h | hj];
+            const T a = x[h], b = x[h | hj];
             const bool swap = desc ? a < b : a > b;
             x[h] = swap ? b : a;
             x[h | hj] = swap ? a : b;
@@ -71,7 +71,7 @@ __device__ __forceinline__ void warp_sort_desc(unsigned long long (&x)[E], int l
 #pragma unroll
         for (int h = 0; h < E; ++h) {
           const int e = lane + 32 * h;
-          const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[h], j);
+          const T y = __shfl_xor_sync(0xffffffffu, x[h], j);
           // the lower index of a descending run keeps the larger value
           const bool take_max = ((e & j) == 0) == ((e & k) == 0);
           x[h] = take_max ? (x[h] > y ? x[h] : y) : (x[h] > y ? y : x[h]);
@@ -302,7 +302,48 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) topk_warp_kernel(const TopkA
   }
   __syncwarp();
   if (n <= 64) {
-    warp_place_sorted<2>(list, n, n, nf, lane, out_ids, out_sc);
+    // When the chosen keys differ only in their low 26 bits or fewer, each
+    // entry sorts as one 32-bit word: those bits, then 63 - its position in
+    // the list (the list is in id order, so equal keys keep the lower id
+    // first); otherwise as (key, id) pairs.
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = lane + 32 * h;
+      if (e < n) {
+        const uint32_t k = (uint32_t)(list[e] >> 32);
+        kmin = min(kmin, k);
+        kmax = max(kmax, k);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    const int vbits = 32 - __clz(kmin ^ kmax);  // 0 when every key is equal
+    if (vbits > 26) {
+      warp_place_sorted<2>(list, n, n, nf, lane, out_ids, out_sc);
+      return;
+    }
+    const uint32_t vmask = (1u << vbits) - 1u;
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = lane + 32 * h;
+      // unused slots sort last: a used one is at least 63 - (n - 1) >= 1
+      w[h] = e < n ? ((((uint32_t)(list[e] >> 32)) & vmask) << 6) | (uint32_t)(63 - e) : 0u;
+    }
+    warp_sort_desc<2>(w, lane);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = lane + 32 * h;  // rank
+      if (r < n) {
+        const unsigned long long x = list[63 - (int)(w[h] & 63u)];
+        out_ids[nf + r] = 0x7fffffff - (int)(uint32_t)(x & 0xffffffffull);
+        out_sc[nf + r] = key_value((uint32_t)(x >> 32));
+      }
+    }
     return;
   }
   for (int j = lane; j < n; j += 32) {

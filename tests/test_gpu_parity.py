@@ -383,6 +383,19 @@ def test_topk_edge_values():
     assert np.array_equal(out.ids, ref.ids)
 
 
+def test_warp_rows_with_all_scores_equal():
+    """Enough short rows for the warp-per-row top-k (3200 rows of at most 157
+    blocks) with every key zero, so every block score ties: each row must
+    choose the lowest ids, in id order."""
+    spec = workloads.small_spec("wz", 505, "bf16", "bf16", R=200, len_range=(1, 20000), topk=20)
+    b = workloads.make_batch(spec)
+    zp = torch.zeros_like(b.payload).cuda()
+    out = _gpu.run(b, planes=(zp, None))
+    zkw = dict(oracle_kwargs(b), payload=np.zeros_like(np_u8(b.payload)))
+    ref = oracle.index.index_step(**zkw)
+    assert np.array_equal(out.ids, ref.ids)
+
+
 @pytest.mark.parametrize("P,G,grid", [(4, 4, 0), (40, 4, 0), (40, 4, 1)])
 def test_bad_page_ids_are_flagged_not_read(P, G, grid):
     """Page ids outside the pool are flagged and not read, on the 16-row path
