@@ -424,6 +424,9 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
   const int V = a.R * TP;
   for (int v = threadIdx.x; v < V; v += blockDim.x) gpre[v] = 0;
   if (threadIdx.x == 0) *cta_flags = 0u;
+  // the first 32 groups' slots, read while the extents are gathered (one
+  // round trip fewer before the first key copy)
+  const int slot_pre = (warp == 0 && lane < V) ? __ldg(a.slot_ids + lane / TP) : 0;
   __syncthreads();
   {
     const int RP = a.R * a.P;
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       int nbk = 0, word = 0;
       if (v < V) {
         const int ext = gpre[v];
-        const int slot = __ldg(a.slot_ids + v / TP);
+        const int slot = v0 == 0 ? slot_pre : __ldg(a.slot_ids + v / TP);
         const bool pad = slot < 0 || slot >= a.n_slots;
         nbk = (pad || ext <= 0) ? 0 : (ext + kBlock - 1) / kBlock;
         const int rem = ext - (nbk - 1) * kBlock;  // tokens in the last block

@@ -27,7 +27,7 @@ def device_planes(batch, dev="cuda"):
 
 
 def run(batch, perrow=False, planes=None, dev="cuda", topk=None, init_blocks=None,
-        local_blocks=None, page_table=None, block_score="max"):
+        local_blocks=None, page_table=None, block_score="max", row_lens=None):
     s = batch.spec
     topk = s.topk if topk is None else topk
     init_blocks = s.init_blocks if init_blocks is None else init_blocks
@@ -45,7 +45,8 @@ def run(batch, perrow=False, planes=None, dev="cuda", topk=None, init_blocks=Non
         fn = idx.idx_score_topk_lse
     else:
         fn = idx.idx_score_topk_perrow if perrow else idx.idx_score_topk
-    fn(q, q_scale, payload, scale, s.k_dtype, pt, batch.slot_ids.to(dev), batch.row_lens.to(dev),
+    lens = batch.row_lens.to(dev) if row_lens is None else row_lens
+    fn(q, q_scale, payload, scale, s.k_dtype, pt, batch.slot_ids.to(dev), lens,
        s.packed_queries, s.gqa, init_blocks, local_blocks, topk, out_ids, out_sc, ws)
     flags = idx.idx_workspace_errors(ws)
     torch.cuda.synchronize()

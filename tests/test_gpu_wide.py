@@ -10,6 +10,7 @@ selections equal except at near ties (tests/_util.compare_row).
 """
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import workloads
@@ -96,6 +97,38 @@ def test_wide_results_do_not_depend_on_the_grid(k_dtype, q_dtype, P, G):
             assert np.array_equal(part.scores.view(np.uint32), full.scores.view(np.uint32))
     finally:
         idx.idx_set_grid_limit(0)
+
+
+@pytest.mark.parametrize("k_dtype,q_dtype", [("bf16", "bf16"), ("nvfp4", "bf16")])
+def test_prefill_extents_from_aligned_and_unaligned_lengths(k_dtype, q_dtype):
+    """A prefill-shaped call's tile extents come from thousands of row lengths,
+    which the ABI takes at any 4-byte alignment.  750 rows a request (not a
+    multiple of 4), 3 heads a row (draft rows cut by tile and pair boundaries),
+    empty rows among them: the lengths read from a 16-byte aligned array and
+    from one that is not agree with the oracle and with each other bit for
+    bit."""
+    rng = np.random.default_rng(441)
+    lens = []
+    for r in range(3):
+        x = rng.integers(1, 4200, size=250)
+        x[rng.random(250) < 0.1] = 0
+        lens.append([int(v) for v in x])
+    spec = workloads.small_spec("w441", 441, k_dtype, q_dtype, R=3, P=250, G=3, init_blocks=1,
+                                local_blocks=2, topk=16, explicit_lens=lens)
+    b = workloads.make_batch(spec)
+    planes = _gpu.device_planes(b)
+    aligned = _gpu.run(b, planes=planes)
+    assert aligned.flags == 0
+    _check(b, aligned, oracle.index.index_step(**oracle_kwargs(b)))
+    dl = b.row_lens.to("cuda").reshape(-1)
+    buf = torch.empty(dl.numel() + 1, dtype=dl.dtype, device="cuda")
+    buf[1:] = dl
+    shifted = buf[1:].view(b.row_lens.shape)
+    assert shifted.data_ptr() % 16 != 0
+    unaligned = _gpu.run(b, planes=planes, row_lens=shifted)
+    assert unaligned.flags == 0
+    assert np.array_equal(unaligned.ids, aligned.ids)
+    assert np.array_equal(unaligned.scores.view(np.uint32), aligned.scores.view(np.uint32))
 
 
 def test_most_rows_per_request():
