@@ -684,7 +684,8 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + L::kCtlOff);
   // ctl[0] = units of the call, ctl[1] = first dynamically scheduled unit,
-  // ctl[2] = dynamic schedule on, ctl[4] = this CTA's device error flags
+  // ctl[2] = dynamic schedule on, ctl[4] = this CTA's device error flags,
+  // ctl[6] = the real group table is built (a hint to the warm-up work)
   unsigned int* cta_flags = reinterpret_cast<unsigned int*>(smem + L::kCtlOff) + 4;
   int* gpre = reinterpret_cast<int*>(smem + L::kGroupOff);  // [V + 1] block prefix
   int* gslot = gpre + kMaxGroups + 1;                      // [V] slot | one-page-last bit
@@ -697,7 +698,10 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
     if (warp == 0) mbar_init(sbase + L::kCtlOff + 32, 1);  // the stall test's barrier
     fence_barrier_init();
   }
-  if (threadIdx.x == 0) prefetch_tensormap(&payload_map);
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&payload_map);
+    ctl[6] = 0;
+  }
 
   // ---- group table: block prefix sums and slots of every group -------------
   // The kernel is launched as a programmatic dependent of whatever ran before
@@ -708,8 +712,10 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   // table of the groups, the others bring every request's page-table row into
   // L2 (one 128-byte line per thread), and then each warp brings the pages of
   // its first static blocks into L2.  A prefetch moves nothing into this CTA
-  // and L2 is coherent, so a stale hint costs only bandwidth.  When nothing
-  // ran before, the hint work overlaps warp 1's and costs no time.
+  // and L2 is coherent, so a stale hint costs only bandwidth.  The warm-up
+  // only pays while the wait holds: once warp 1 has built the real table
+  // (nothing ran before, or it has finished) the other warps drop what is left
+  // of it and start on their blocks.
   // NVFP4 calls are bound by the key decode, not by HBM, and measured slower
   // with the hint work: they wait first and warm only the page table.
   const int V = a.perrow ? a.R * a.P : a.R;
@@ -731,14 +737,21 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
   } else if (warp == 1) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     build_groups<KF, false>(a, gpre, gslot, ctl, cta_flags, V, lane);
+    __syncwarp();
+    if (lane == 0) ctl[6] = 1;
   } else {
     int* hpre = reinterpret_cast<int*>(smem + L::kHintOff);  // [V + 1]
     int* hslot = hpre + kHintGroups + 1;                     // [V]
     volatile int* hctl = hslot + kHintGroups;                // units, first dynamic unit
     const bool hinted = V <= kHintGroups;
     if (warp == 0) {
-      if (hinted) build_groups<KF, true>(a, hpre, hslot, hctl, nullptr, V, lane);
-    } else {
+      if (hinted) {
+        if (!__any_sync(0xffffffffu, ctl[6] != 0))
+          build_groups<KF, true>(a, hpre, hslot, hctl, nullptr, V, lane);
+        else if (lane == 0)
+          hctl[0] = 0;  // no blocks to warm
+      }
+    } else if (ctl[6] == 0) {
       const int lines_per = (a.max_pages + 31) / 32;
       const int nthr = (int)gridDim.x * (NC - 2) * 32;
       const int gt = ((int)blockIdx.x * (NC - 2) + warp - 2) * 32 + lane;
@@ -759,6 +772,7 @@ __global__ void __launch_bounds__(Layout<KF>::kThreads, 1)
       // unit sh0 + w + j NC), spread over the NC - 1 warps here
       const int rank = warp == 0 ? 0 : warp - 1;
       for (int k = rank; k < NC * kPrefetchUnits; k += NC - 1) {
+        if (__any_sync(0xffffffffu, ctl[6] != 0)) break;
         const int u = sh0 + k;
         if (u < sh1 && u < Uh) {
           int v, b;
