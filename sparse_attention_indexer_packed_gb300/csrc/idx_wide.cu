@@ -14,19 +14,21 @@
 //
 // Roles inside a CTA (one CTA per SM, persistent over a contiguous range of
 // blocks of the flattened (group, block) list):
-//   warp 0      TMA producer: the group's query tiles (bf16 / e4m3) and each
-//               block's two key pages (+ their scales) into a ring of stages;
+//   warp 0      TMA producer: the group's query tiles (bf16, e4m3, or for
+//               NVFP4 keys the f16 rows q16_kernel made) and each block's two
+//               key pages (+ their scales) into a ring of stages;
 //   warp 1      allocates 512 TMEM columns (one 128-column fp32 accumulator
-//               per tile of a pair, two blocks in flight); lane 0 issues both
-//               tiles' MMAs of a block against the same staged keys and commits
-//               them to mbarriers;
+//               per tile of a pair, two blocks in flight); as a whole warp it
+//               waits for the operands and one elected lane issues both tiles'
+//               MMAs of a block against the same staged keys and commits them
+//               to mbarriers;
 //   warps 2..9  epilogue, group g (four warps) owning tile g of the pair:
 //               thread = tile row; tcgen05.ld of its 128 scores, the row's mask
 //               and block score, one workspace write per row;
 //   warps 10..13 (NVFP4 keys) decode a block's e2m1 codes x E4M3 group scales
 //               into an f16 operand tile (ROCm/ATOM #2745: the products are
-//               exact); each epilogue group also converts its bf16 query tile
-//               to f16 with a per-row power-of-two scale, undone on the result.
+//               exact); the query rows are scaled by a power of two per row
+//               into f16 range by q16_kernel, undone on the result.
 // Every wait is bounded; a timeout sets IDX_DEVERR_TIMEOUT and the CTA winds down
 // (copies in flight are waited for, TMEM is freed).
 #include <cuda_bf16.h>
