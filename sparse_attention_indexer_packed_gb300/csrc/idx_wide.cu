@@ -99,8 +99,9 @@ struct WLayout {
   static constexpr int kDecOff = kStageOff + S * C::kStageBytes;
   static constexpr int kScaleOff = kDecOff + SD * 32768;
   static constexpr int kBarOff = kScaleOff + S * 2 * C::kPageScale;
-  // full[S] empty[S] dfull[SD] dempty[SD] afull[kUnits] aempty[kUnits] qfull qempty done
-  static constexpr int kNumBars = 2 * S + 2 * SD + 2 * kUnits + 3;
+  // full[S] empty[S] dfull[SD] dempty[SD] afull[kUnits] aempty[kUnits] qfull[2]
+  // qempty[2] done
+  static constexpr int kNumBars = 2 * S + 2 * SD + 2 * kUnits + 5;
   static constexpr int kCtlOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kGroupOff = kCtlOff + 64;
   static constexpr int kBytes = kGroupOff + (2 * kMaxGroups + 1) * 4;
@@ -126,14 +127,15 @@ struct WLayout {
   __device__ static uint32_t aempty(uint32_t sb, int j) {
     return sb + kBarOff + 8 * (2 * S + 2 * SD + kUnits + j);
   }
-  __device__ static uint32_t qfull(uint32_t sb) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits);
+  // query slot k's barriers (k = 0 only, unless every group is one tile)
+  __device__ static uint32_t qfull(uint32_t sb, int k) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + k);
   }
-  __device__ static uint32_t qempty(uint32_t sb) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + 1);
+  __device__ static uint32_t qempty(uint32_t sb, int k) {
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + 2 + k);
   }
   __device__ static uint32_t done(uint32_t sb) {
-    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + 2);
+    return sb + kBarOff + 8 * (2 * S + 2 * SD + 2 * kUnits + 4);
   }
 };
 
@@ -398,8 +400,10 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       mbar_init(L::afull(sb, j), 1);
       mbar_init(L::aempty(sb, j), 8);  // both epilogue groups, every block
     }
-    mbar_init(L::qfull(sb), 1);
-    mbar_init(L::qempty(sb), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(L::qfull(sb, k), 1);
+      mbar_init(L::qempty(sb, k), 1);
+    }
     mbar_init(L::done(sb), 1);
     mbar_init(sb + L::kCtlOff + 32, 1);  // the stall test's barrier
     fence_barrier_init();
@@ -479,6 +483,14 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
   const uint32_t tmem = (uint32_t)ctl[1];
   const int u0 = (int)((long long)U * blockIdx.x / gridDim.x);
   const int u1 = (int)((long long)U * (blockIdx.x + 1) / gridDim.x);
+  // Query tiles: a group's tiles go to the two slots of shared memory, and
+  // the next group's are loaded once the MMAs of this one are done with them.
+  // When every group is a single tile (up to 128 rows a request, a verify
+  // pack) the groups alternate between the slots instead: the n-th group's
+  // tile goes to slot n % 2, so the next group's rows load while the MMAs
+  // still read the other slot and a CTA whose range crosses a group boundary
+  // does not drain its MMAs there.
+  const bool alt = a.tiles == 1;
 
   if (warp == 0) {
     // ======================= producer =======================
@@ -503,21 +515,26 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       const int p1 = __shfl_sync(0xffffffffu, wpg, 2 * k + 1);
       if (v != prev_v) {
         if (lane == 0) {
-          // the previous pair's MMAs must be done with the query tiles
-          if (nq > 0 && !mbar_wait_bounded(L::qempty(sb), (nq - 1) & 1, a.wait_ns)) ok = false;
+          // the MMAs of the slot's previous group must be done with it
+          const int k = alt ? (nq & 1) : 0;
+          const int prev = alt ? nq - 2 : nq - 1;  // the slot's previous load
+          if (prev >= 0 &&
+              !mbar_wait_bounded(L::qempty(sb, k), (alt ? prev >> 1 : prev) & 1, a.wait_ns))
+            ok = false;
           if (ok) {
             const int r = v / TP;
             const int tile0 = 2 * (v - r * TP);
             const int nt = min(kPair, a.tiles - tile0);
-            mbar_arrive_expect_tx(L::qfull(sb), nt * C::kQBytes);
+            const uint32_t qb = L::qfull(sb, k);
+            mbar_arrive_expect_tx(qb, nt * C::kQBytes);
             for (int t = 0; t < nt; ++t) {
               const int base_row = r * a.M + (tile0 + t) * kWRows;
-              const uint32_t qt = qtile + t * C::kQBytes;
+              const uint32_t qt = qtile + (k + t) * C::kQBytes;
               if (KF != kFp8) {  // bf16 rows, or the f16 rows made for NVFP4 keys
-                tma_load_2d(qt, &qmap, 0, base_row, L::qfull(sb));
-                tma_load_2d(qt + 16384, &qmap, 64, base_row, L::qfull(sb));
+                tma_load_2d(qt, &qmap, 0, base_row, qb);
+                tma_load_2d(qt + 16384, &qmap, 64, base_row, qb);
               } else {
-                tma_load_2d(qt, &qmap, 0, base_row, L::qfull(sb));
+                tma_load_2d(qt, &qmap, 0, base_row, qb);
               }
             }
           }
@@ -562,7 +579,10 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
       // when another role gave up early (instant when they were all consumed)
       for (int k = max(0, i - S); k < i; ++k)
         (void)mbar_wait_bounded(L::full(sb, k % S), (k / S) & 1, 200000000ull);
-      if (nq > 0) (void)mbar_wait_bounded(L::qfull(sb), (nq - 1) & 1, 200000000ull);
+      // (the last load of each slot used)
+      for (int n = max(0, nq - (alt ? 2 : 1)); n < nq; ++n)
+        (void)mbar_wait_bounded(L::qfull(sb, alt ? (n & 1) : 0), (alt ? n >> 1 : n) & 1,
+                                200000000ull);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -570,7 +590,8 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
     // issues each MMA and commit (tc_*_warp).  Every wait is taken by all lanes
     // and its outcome agreed with a vote, so the warp stays converged.
     {
-      int prev_v = -1, nq = 0, i = 0, nt = 1;
+      int prev_v = -1, nq = 0, i = 0, nt = 1, qk = 0;
+      uint32_t qbase = qtile;  // the group's query slot
       bool ok = true;
       int v = 0, b = 0;
       if (u0 < u1) wlocate(gpre, V, u0, v, b);
@@ -578,9 +599,12 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         if (v != prev_v) {
           // stall test: the first wait goes to a barrier nothing completes
           const bool stall = a.stall_test && nq == 0;
+          qk = alt ? (nq & 1) : 0;
+          qbase = qtile + qk * C::kQBytes;
           if (!__all_sync(0xffffffffu,
-                          mbar_wait_bounded(stall ? sb + L::kCtlOff + 32 : L::qfull(sb),
-                                            stall ? 0u : nq & 1, a.wait_ns))) {
+                          mbar_wait_bounded(stall ? sb + L::kCtlOff + 32 : L::qfull(sb, qk),
+                                            stall ? 0u : (alt ? nq >> 1 : nq) & 1,
+                                            a.wait_ns))) {
             ok = false;
             break;
           }
@@ -615,7 +639,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         // both tiles of the pair against the same staged keys
         for (int t = 0; t < nt; ++t) {
           const uint32_t d_tmem = tmem + (uint32_t)((j * kPair + t) * 128);
-          const uint32_t qt = qtile + t * C::kQBytes;
+          const uint32_t qt = qbase + t * C::kQBytes;
           if (KF == kFp8) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -636,7 +660,7 @@ __global__ void __launch_bounds__(WLayout<KF>::kThreads, 1)
         int vn = v, bn = b;
         if (u + 1 < u1) wnext(gpre, V, vn, bn);
         else vn = -1;
-        if (vn != v) tc_commit_warp(L::qempty(sb));  // last block of this pair
+        if (vn != v) tc_commit_warp(L::qempty(sb, qk));  // last block of this group
         v = vn;
         b = bn;
       }

@@ -495,15 +495,18 @@ def test_topk_warp_rows_match_cta_rows(topk, max_len):
 
 
 @pytest.mark.parametrize("k_dtype,q_dtype,P,G", [("bf16", "bf16", 4, 4), ("bf16", "bf16", 40, 4),
+                                                 ("bf16", "bf16", 8, 8),
                                                  ("fp8_e4m3", "fp8_e4m3", 8, 8),
-                                                 ("nvfp4", "bf16", 40, 4)])
+                                                 ("nvfp4", "bf16", 40, 4),
+                                                 ("nvfp4", "bf16", 8, 8)])
 def test_wait_timeout_is_reported_and_the_context_survives(k_dtype, q_dtype, P, G):
     """A wait that nothing completes (the stall test: one role per score CTA
     waits on a barrier no one arrives at, with a 20 ms limit) must end the call
     through the timeout path -- copies in flight waited for, TMEM freed,
     IDX_DEVERR_TIMEOUT in the workspace -- instead of hanging or faulting, and
     the next call must be exact again.  P x G = 40 x 4 takes the tensor-core
-    path, whose other roles then also run out of their waits."""
+    path, whose other roles then also run out of their waits; 8 x 8 is one
+    tile per request there, whose query slots alternate."""
     import sparse_attention_indexer_packed_gb300 as idx
     spec = workloads.small_spec("to", 701, k_dtype, q_dtype, R=4, P=P, G=G,
                                 len_range=(2000, 9000), topk=16)
