@@ -41,12 +41,16 @@ def build_library(verbose: bool = False, force: bool = False) -> str:
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(HERE, "..", "include", "idx.h"))
+    # every output is written under a name of this process's own and then
+    # renamed into place, so builders running at once (one per rank of a
+    # multi-GPU run) never read or link a half-written file
+    tag = f".{os.getpid()}.tmp"
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
         o = os.path.join(BUILD, src.replace(".cu", ".o"))
         if force or _stale(o, [s] + headers):
-            jobs.append([nvcc, *ARCH, *FLAGS, "-c", s, "-o", o])
+            jobs.append(([nvcc, *ARCH, *FLAGS, "-c", s, "-o", o + tag], o))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -56,11 +60,16 @@ def build_library(verbose: bool = False, force: bool = False) -> str:
             print(r.stdout + r.stderr)
         return r
 
+    def compile_one(job):
+        cmd, out = job
+        run(cmd)
+        os.replace(out + tag, out)
+
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        list(ex.map(run, jobs))
+        list(ex.map(compile_one, jobs))
     objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
     if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+        tmp = LIB + tag
         run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     return LIB
