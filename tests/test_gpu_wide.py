@@ -47,6 +47,7 @@ for k_dtype, q_dtype in [("bf16", "bf16"), ("fp8_e4m3", "fp8_e4m3"), ("nvfp4", "
         (403, 3, (50, 3), (1, 3000), (), 2, 2, 8),        # 150 rows: a tile cuts a draft row
         (404, 2, (256, 2), (4000, 4500), (), 1, 4, 64),   # prefill chunk: 256 query tokens
         (405, 3, (75, 4), (100, 6000), (0,), 1, 2, 16),   # 300 rows: a tile pair + a lone tile
+        (406, 5, (8, 8), (1, 5000), (1, 2), 1, 2, 16),    # one tile a request, two pad requests
     ]:
         CASES.append(pytest.param(k_dtype, q_dtype, seed, R, P, G, lens, pads, init, local, topk,
                                   id=f"{k_dtype}-{seed}-P{P}G{G}"))
